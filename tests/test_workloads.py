@@ -1,0 +1,90 @@
+"""The seeded input generators: shapes, determinism, layout and the stated
+distributions (checked statistically), at reduced sizes."""
+import numpy as np
+
+from moe_swiglu_epilogue_gb300 import workloads as W
+
+
+def test_bf16_rounding_is_nearest_even():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -9, -2.5, 0.0, -0.0],
+                 np.float32)
+    b = W.bf16_bits(x)
+    # 1 + 2^-8 is a tie -> even (1.0); 1 + 3*2^-8 is a tie -> 1 + 2^-6
+    assert b.tolist() == [0x3F80, 0x3F80, 0x3F82, 0x3F80, 0xC020, 0x0000, 0x8000]
+    assert np.array_equal(W.bf16_to_f32(b)[:2], np.array([1.0, 1.0], np.float32))
+
+
+def test_interleave_layout():
+    gate = np.arange(32, dtype=np.uint16).reshape(1, 32)
+    up = (1000 + np.arange(32, dtype=np.uint16)).reshape(1, 32)
+    gu = W.interleave_gate_up(gate, up)[0]
+    assert gu[:8].tolist() == list(range(8))
+    assert gu[8:16].tolist() == list(range(1000, 1008))
+    assert gu[16:24].tolist() == list(range(8, 16))
+    mask = W.gate_column_mask(32)
+    assert np.all(gu[mask] < 1000) and np.all(gu[~mask] >= 1000)
+
+
+def test_deterministic_and_chunk_independent():
+    a = W.quantize_normal(rows=300, K=64, seed=0).data
+    b = W.quantize_normal(rows=300, K=64, seed=0).data
+    c = W.quantize_normal(rows=300, K=64, seed=1).data
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
+
+
+def test_quantize_normal_distribution():
+    w = W.quantize_normal(rows=128, K=2048, seed=0)
+    x = W.bf16_to_f32(w.data)
+    assert w.data.shape == (128, 2048)
+    assert abs(x.mean()) < 0.02 and abs(x.std() - 1.0) < 0.02
+
+
+def test_fused_gate_and_up_sigmas():
+    w = W.fused_normal(rows=256, I=512)
+    v = W.bf16_to_f32(w.data)
+    m = W.gate_column_mask(512)
+    assert abs(v[:, m].std() - 2.0) < 0.05 and abs(v[:, ~m].std() - 1.0) < 0.03
+    assert w.clamp_L == 7.0
+
+
+def test_routing_offsets():
+    off = W.routing_offsets(4096, 256, 8, seed=2)
+    assert off.dtype == np.int32 and off.shape == (257,)
+    assert off[0] == 0 and off[-1] == 32768 and np.all(np.diff(off) >= 0)
+    counts = np.diff(off)
+    assert abs(counts.mean() - 128) < 1e-9 and counts.std() < 25
+    w = W.ragged_routing(tokens=64, experts=16, topk=4, I=64, pad_rows=5)
+    assert w.rows == 64 * 4 + 5 and w.active_rows == 256
+
+
+def test_prefill_heavy_tail_structure():
+    w = W.prefill_heavy_tail(rows=512, I=768)
+    v = W.bf16_to_f32(w.data).reshape(512, 768 // 16, 32)
+    zero_blocks = np.all(v == 0, axis=2).mean()
+    assert 0.04 < zero_blocks < 0.06
+    # |v| > 60 is almost only an x100 outlier with |t3| > 1.2 (P ~ 0.32):
+    # 1e-3 * 0.32 * 0.95 (zeroed blocks) ~ 3e-4
+    big = (np.abs(v) > 60).mean()
+    assert 1.5e-4 < big < 6e-4
+    assert w.clamp_L == 10.0
+
+
+def test_edge_kinds_present():
+    w = W.edge_structured(rows=256, I=512)
+    kinds = w.meta["kinds"]
+    frac = (kinds > 0).mean()
+    assert 0.08 < frac < 0.12
+    assert set(np.unique(kinds)) == set(range(len(W.EDGE_KINDS) + 1))
+    v = W.bf16_to_f32(w.data).reshape(256, 512 // 16, 2, 2, 8)
+    zero_ups = v[kinds == 1][:, :, 1, :]
+    assert np.all(zero_ups == 0) and np.any(np.signbit(zero_ups))
+    sat = v[kinds == 2]
+    assert np.all(sat[:, :, 0, :] >= 7.0) and np.all(np.abs(sat[:, :, 1, :]) < 0.03)
+    assert np.all(np.isfinite(W.bf16_to_f32(w.data)))
+
+
+def test_algorithmic_bytes():
+    w = W.fused_normal(rows=4, I=2048)
+    assert w.algorithmic_bytes() == 4 * 9344
+    q = W.quantize_normal(rows=4, K=2048)
+    assert q.algorithmic_bytes() == 4 * 5248
