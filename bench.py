@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the fused deinterleave + clamped SwiGLU + NVFP4 quantize step.
+
+One step = one call of moe_swiglu_nvfp4_quantize (one kernel launch) over the
+MoE decode/routing workload: 4096 tokens x top-8 of 256 experts = 32768 rows
+in per-expert segments (device offsets), I = 2048, BF16 gate/up ~ N(0, 1.5^2),
+L = 7. Inputs (306 MB) are larger than L2 (129 MB), and two input copies
+alternate between steps. Metric: algorithmic GB/s (BF16 read + FP4 + scale
+written) and rows/s; the roofline is HBM bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. Under torchrun (N > 1) every rank runs its own
+copy of the workload (weak scaling, no data-path collective); the only
+collectives are the barrier around the timed region and the max over ranks of
+its duration.
+
+--impl reference times the CPU oracle (test infrastructure, single-threaded
+C) on a bounded sample of the same workload on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused SwiGLU+NVFP4 quant GB/s (rows/s) and % of GB300 HBM peak, 1 GPU"
+UNIT = "GB/s"
+HEADLINE = "ragged"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host side; tested with gloo on CPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(seconds: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return seconds
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def aggregate_throughput(bytes_per_step: int, rows_per_step: int, steps: int,
+                         max_seconds: float, world: int) -> dict:
+    """Whole-job throughput: every rank processed its own batch each step."""
+    return {
+        "gbs": world * bytes_per_step * steps / max_seconds / 1e9,
+        "rows_per_s": world * rows_per_step * steps / max_seconds,
+        "ms_per_step": max_seconds * 1e3 / steps,
+    }
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("moe_swiglu_epilogue_gb300/csrc/moe_nvfp4.cu", "include/moe_nvfp4.h"):
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; None otherwise."""
+    p = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh)
+    for r in rec.get("records", []):
+        if (r.get("kernel") == kernel and r.get("workload") == workload
+                and r.get("source_hash") == kernel_source_hash()):
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+class DirectCall:
+    """Pre-marshalled C-ABI call (the binding's work done once), so the host
+    enqueues launches faster than the ~50 us kernels run."""
+
+    def __init__(self, fn, args):
+        self.fn = fn
+        self.args = args
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != 0:
+            raise RuntimeError(f"C-ABI call failed with code {rc}")
+
+
+def make_call(lib, w, src, packed, sf, off, stream):
+    P = ctypes.c_void_p
+    s = P(stream.cuda_stream)
+    if w.kind == "quantize":
+        return DirectCall(lib.moe_nvfp4_quantize,
+                          (P(src.data_ptr()), w.rows, w.width, P(packed.data_ptr()),
+                           P(sf.data_ptr()), s))
+    E = 0 if off is None else off.shape[0] - 1
+    return DirectCall(lib.moe_swiglu_nvfp4_quantize,
+                      (P(src.data_ptr()), w.rows, w.width, ctypes.c_float(w.clamp_L),
+                       P(0 if off is None else off.data_ptr()), ctypes.c_int32(E),
+                       P(packed.data_ptr()), P(sf.data_ptr()), s))
+
+
+def device_buffers(w, torch, copies: int):
+    srcs = [torch.from_numpy(w.data.view(np.int16)).cuda() for _ in range(copies)]
+    packed = torch.empty((w.rows, w.width // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((w.rows, w.width // 16), dtype=torch.uint8, device="cuda")
+    off = None if w.offsets is None else torch.from_numpy(w.offsets).cuda()
+    return srcs, packed, sf, off
+
+
+def time_steps(torch, calls, steps: int, warmup: int, stream, flush=None):
+    """Warm up, then time exactly `steps` launches: total device time between
+    two events, plus each launch's own duration (event pairs on the launching
+    stream). `flush` (if given) runs between launches, outside the pairs."""
+    for i in range(warmup):
+        calls[i % len(calls)]()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_begin.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        starts[i].record(stream)
+        calls[i % len(calls)]()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    total_s = t_begin.elapsed_time(t_end) / 1e3
+    per = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    return total_s, per, wall0, wall1
+
+
+def run_workload(torch, lib, M, W, name: str, steps: int, warmup: int, stream, copies=2,
+                 cold_small=False):
+    w = W.make(name)
+    srcs, packed, sf, off = device_buffers(w, torch, copies)
+    calls = [make_call(lib, w, s, packed, sf, off, stream) for s in srcs]
+    flush = None
+    if cold_small:
+        scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+        flush = lambda: scratch.fill_(1)       # evict the small input from L2
+    with torch.cuda.stream(stream):
+        total_s, per, w0, w1 = time_steps(torch, calls, steps, warmup, stream, flush)
+    return w, total_s, per, w0, w1, (srcs, packed, sf, off)
+
+
+def e2e_measure(torch, lib, w, stream, steps: int):
+    """Through the public API with HOST buffers: each step copies the input
+    from pinned host memory, runs the C-ABI call, copies the outputs back."""
+    P = ctypes.c_void_p
+    h_in = torch.from_numpy(w.data.view(np.int16)).pin_memory()
+    h_packed = torch.empty((w.rows, w.width // 2), dtype=torch.uint8).pin_memory()
+    h_sf = torch.empty((w.rows, w.width // 16), dtype=torch.uint8).pin_memory()
+    d_in = torch.empty_like(h_in, device="cuda")
+    d_packed = torch.empty_like(h_packed, device="cuda")
+    d_sf = torch.empty_like(h_sf, device="cuda")
+    h_off = None if w.offsets is None else torch.from_numpy(w.offsets).pin_memory()
+    d_off = None if h_off is None else torch.empty_like(h_off, device="cuda")
+    call = make_call(lib, w, d_in, d_packed, d_sf, d_off, stream)
+
+    def step():
+        d_in.copy_(h_in, non_blocking=True)
+        if d_off is not None:
+            d_off.copy_(h_off, non_blocking=True)
+        call()
+        h_packed.copy_(d_packed, non_blocking=True)
+        h_sf.copy_(d_sf, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        barrier()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    secs = ev0.elapsed_time(ev1) / 1e3
+    h2d = h_in.numel() * 2 + (0 if h_off is None else h_off.numel() * 4)
+    d2h = h_packed.numel() + h_sf.numel()
+    return secs, h2d, d2h
+
+
+def describe(w) -> str:
+    if w.name == "ragged":
+        return (f"ragged: {w.meta['tokens']} tokens x top-{w.meta['topk']} of "
+                f"{w.meta['experts']} experts = {w.active_rows} rows in per-expert segments "
+                f"(device offsets), I={w.width}, gate/up BF16 ~ N(0,1.5^2), L={w.clamp_L}")
+    what = "quantize-only x" if w.kind == "quantize" else "fused gu"
+    extra = "" if w.kind == "quantize" else f", L={w.clamp_L}"
+    return f"{w.name}: {what} [{w.rows}, {w.width}]{extra}"
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The oracle, as it stands (single-threaded C), on a bounded sample of
+    the workload: whole active rows in order until ~budget_s of CPU work."""
+    import oracle
+    oracle.build()
+    r0 = 0 if w.offsets is None else int(w.offsets[0])
+    r1 = w.rows if w.offsets is None else int(w.offsets[-1])
+    per_row = (2 * w.width if w.kind == "quantize" else 4 * w.width) + w.width // 2 + w.width // 16
+    t = time.perf_counter()
+    probe = w.data[r0:r0 + 64]
+    if w.kind == "quantize":
+        oracle.quantize_nvfp4(probe)
+    else:
+        oracle.swiglu_quantize_nvfp4(probe, w.clamp_L)
+    per_row_s = (time.perf_counter() - t) / 64
+    n = int(min(r1 - r0, max(64, budget_s / max(per_row_s, 1e-9))))
+    sample = w.data[r0:r0 + n]
+    t = time.perf_counter()
+    if w.kind == "quantize":
+        oracle.quantize_nvfp4(sample)
+    else:
+        oracle.swiglu_quantize_nvfp4(sample, w.clamp_L)
+    secs = time.perf_counter() - t
+    return {"value": per_row * n / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {r1 - r0} active rows of the {w.name} workload "
+                      f"(I={w.width}), one pass, {secs:.2f} s",
+            "rows_per_s": n / secs}
+
+
+def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str, traffic):
+    mean_s = statistics.fmean(per_launch_s)
+    achieved = bytes_per_launch / mean_s / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
+            "peak_source": f"{peak_src} (hbm_gbs, burst copy)",
+            "launch_us_mean": round(mean_s * 1e6, 2),
+            "launch_us_median": round(statistics.median(per_launch_s) * 1e6, 2)}
+
+
+def main_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    import moe_swiglu_epilogue_gb300 as M
+    from moe_swiglu_epilogue_gb300 import build, workloads as W
+    if rank == 0 or world == 1:
+        build.build()
+    barrier()
+    lib = M.load_library()
+    stream = torch.cuda.Stream()
+    peak, peak_src = measured_peaks()
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    gpu_id = visible[local] if local < len(visible) else str(local)
+
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    w, total_s, per, w0, w1, _keep = run_workload(torch, lib, M, W, args.workload, args.steps,
+                                                  args.warmup, stream)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+    del _keep
+    max_s = max_over_ranks(total_s)
+    agg = aggregate_throughput(w.algorithmic_bytes(), w.active_rows, args.steps, max_s, world)
+
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    e2e_s, h2d, d2h = e2e_measure(torch, lib, w, stream, e2e_steps)
+    e2e_max = max_over_ranks(e2e_s)
+    e2e = {"value": round(world * w.algorithmic_bytes() * e2e_steps / e2e_max / 1e9, 2),
+           "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": e2e_steps, "rows_per_s": round(world * w.active_rows * e2e_steps / e2e_max, 1)}
+
+    kernel = "nvfp4_quantize_kernel" if w.kind == "quantize" else "swiglu_nvfp4_kernel"
+    roof = roofline(w.algorithmic_bytes(), per, peak, peak_src, recorded_traffic(kernel, w.name))
+
+    others = {}
+    if not args.no_extra:
+        for name, cold in (("fused", True), ("prefill", False), ("quantize", True),
+                           ("prefill_quantize", False)):
+            if name == args.workload:
+                continue
+            steps = min(args.steps, 200)
+            ww, tot, per_o, _, _, keep = run_workload(torch, lib, M, W, name, steps,
+                                                      min(args.warmup, 20), stream,
+                                                      copies=1 if cold else 2, cold_small=cold)
+            del keep
+            torch.cuda.empty_cache()
+            mean_s = statistics.fmean(per_o)
+            others[name] = {
+                "rows": ww.rows, "width": ww.width, "kind": ww.kind,
+                "gbs": round(ww.algorithmic_bytes() / mean_s / 1e9, 1),
+                "frac_of_peak": round(ww.algorithmic_bytes() / mean_s / 1e9 / peak, 4),
+                "launch_us_mean": round(mean_s * 1e6, 2),
+                "l2": "flushed before every launch" if cold else "inputs larger than L2",
+            }
+
+    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(agg["gbs"], 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": describe(w),
+                   "rows": w.rows, "width": w.width, "experts": w.meta.get("experts"),
+                   "bytes_per_step": w.algorithmic_bytes(),
+                   "l2": f"inputs ({w.data.nbytes / 1e6:.0f} MB) larger than L2 (129 MB); "
+                         "2 input copies alternate",
+                   "parallelism": f"{world} independent replica(s), no collective on the path"},
+        "rows_per_s": round(agg["rows_per_s"], 1),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "workloads": others,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main_reference(args):
+    """The oracle on the host cores, same metric and workload, bounded
+    per-step sample; rank 0 only."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from moe_swiglu_epilogue_gb300 import workloads as W
+    oracle.build()
+    w = W.make(args.workload)
+    r0 = 0 if w.offsets is None else int(w.offsets[0])
+    r1 = w.rows if w.offsets is None else int(w.offsets[-1])
+    per_row = w.algorithmic_bytes() // max(1, w.active_rows)
+
+    def run(a, n):
+        if w.kind == "quantize":
+            oracle.quantize_nvfp4(w.data[a:a + n])
+        else:
+            oracle.swiglu_quantize_nvfp4(w.data[a:a + n], w.clamp_L)
+
+    t = time.perf_counter()
+    run(r0, 32)
+    per_row_s = (time.perf_counter() - t) / 32
+    budget = args.reference_budget_s
+    n = int(max(1, min(r1 - r0, budget / (args.steps + args.warmup) / max(per_row_s, 1e-9))))
+    for i in range(args.warmup):
+        run(r0 + (i * n) % max(1, r1 - r0 - n + 1), n)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        run(r0 + (i * n) % max(1, r1 - r0 - n + 1), n)
+    secs = time.perf_counter() - t
+    value = per_row * n * args.steps / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (oracle)",
+        "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": describe(w), "rows_per_step_sample": n},
+        "rows_per_s": round(n * args.steps / secs, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n} consecutive active rows per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=["ragged", "fused", "prefill", "edge", "quantize", "prefill_quantize"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--reference-budget-s", type=float, default=90.0)
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

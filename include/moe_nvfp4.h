@@ -1,0 +1,153 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_swiglu_nvfp4.so, the GB300 (sm_103a)
+ * kernels for the MoE expert activation step between the L1 and L2 GEMMs:
+ * deinterleave the L1 output, clamped SwiGLU, NVFP4 quantize.
+ *
+ * Source of the operations (nvfp4-megamoe-kernel project pages):
+ *  - "NVFP4-1.1 Approach Update", section "Revised approach: Compact SwiGLU
+ *    output": the L1 GEMM writes BF16 column groups [gate*8, swiglu*8, ...];
+ *    a deinterleave + quantize kernel turns them into x2-packed FP4
+ *    (tokens, I/2) plus FP8 E4M3 scales (tokens, I/16); the compact plan
+ *    quantizes a plain BF16 (tokens, I) tensor instead (quantize-only).
+ *  - "2026-05-28 Status", commit "NVFP4-1.1: FP4 quantization primitives":
+ *    E4M3 with bias 7, exponents 0-15, exp 15 / mant 7 NaN (max 448),
+ *    subnormals m * 2^-9, round-to-nearest-even with mantissa carry; the
+ *    half-step index 0..12 -> E2M1 index 0..7; per-element quantize + sign +
+ *    pack. Table "What's DONE and PROVEN": SwiGLU clamping in the kernel.
+ *  - "NVFP4-1.1 Approach, Part 2": the RNE half-step fix (s = 5.25 -> nibble
+ *    6) and 16 values -> 8 packed bytes + 1 scale byte per block.
+ *
+ * What every call computes, per row and per block of 16 consecutive outputs:
+ *    y_i   = the fp32 value of silu(min(g_i, L)) * clamp(u_i, -L, L),
+ *            silu(a) = a / (1 + exp(-a))     (quantize-only: y_i = x_i)
+ *    amax  = max |y_i|;   sf = E4M3_RNE_saturating(amax / 6)
+ *    s_i   = y_i / value(sf)   (+-0 with the sign of y_i when sf == 0)
+ *    h_i   = round_half_even(2 * min(|s_i|, 6))            in 0..12
+ *    nib_i = {0,1,2,3,4,4,5,6,6,6,6,7,7}[h_i] | (sign(s_i) ? 8 : 0)
+ *    packed[row, c/2] = nib(c even) | nib(c odd) << 4;  sf[row, c/16] = sf
+ * The fp32 value y_i is the double-precision evaluation of the formula
+ * rounded once to fp32. The fused kernel computes y_i with fast fp32
+ * arithmetic (relative error far below the window below) and, wherever a
+ * fast value lies within the window of a rounding boundary of the scale or
+ * of a nibble, re-evaluates it in double precision, so its scale and nibble
+ * decisions are those of the definition. Quantize-only is exact throughout.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *    rows contiguous (leading dimension = width). Nothing is allocated,
+ *    freed or synchronised; the work is launched on `stream` (a
+ *    cudaStream_t; NULL = the legacy default stream) and the call returns
+ *    without waiting for it.
+ *  - Input pointers must be 32-byte aligned (256-bit loads); `packed` and
+ *    `sf` must be 16-byte aligned.
+ *  - Return 0 on success or a negative MOE_NVFP4_E* code; arguments are
+ *    checked on the host before any launch, so a rejected call launches
+ *    nothing and leaves the outputs untouched. Faults inside a launched
+ *    kernel surface, as with any CUDA launch, at the caller's next
+ *    synchronisation.
+ *  - The library caches, per device, the SM count and the kernels'
+ *    occupancy on first use; it is otherwise stateless and thread-safe.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The library is built with hidden visibility; these are its only exports. */
+#if defined(__GNUC__)
+#define MOE_NVFP4_API __attribute__((visibility("default")))
+#else
+#define MOE_NVFP4_API
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *moe_nvfp4_stream_t;
+
+enum {
+    MOE_NVFP4_OK = 0,
+    MOE_NVFP4_ENULL = -1,       /* a required pointer is NULL while rows > 0 */
+    MOE_NVFP4_EWIDTH = -2,      /* K or I is not a positive multiple of 16 */
+    MOE_NVFP4_EALIGN = -3,      /* a pointer breaks the alignment rule above */
+    MOE_NVFP4_ESIZE = -4,       /* rows < 0, or a byte count overflows int64 */
+    MOE_NVFP4_ECLAMP = -5,      /* clamp_L not finite, not > 0, or > 2^64 */
+    MOE_NVFP4_EOFFSETS = -6,    /* num_experts < 0, or offsets NULL with num_experts > 0 */
+    MOE_NVFP4_ELAUNCH = -7,     /* the CUDA launch (or a device query) failed */
+};
+
+/*
+ * Quantize-only (the pages' quantize_nvfp4_gpu; the "compact" flow):
+ *   x      BF16 [rows, K]      (uint16 bit patterns)
+ *   packed uint8 [rows, K/2]   two E2M1 nibbles per byte, even column low
+ *   sf     uint8 [rows, K/16]  FP8 E4M3 scale codes (torch.float8_e4m3fn)
+ * Bit-exact with the definition above for every finite input.
+ */
+MOE_NVFP4_API int moe_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K,
+                       uint8_t *packed, uint8_t *sf, moe_nvfp4_stream_t stream);
+
+/*
+ * Fused deinterleave + clamped SwiGLU + quantize (the pages'
+ * deinterleave_quantize_nvfp4_cuda with the SwiGLU math in the kernel):
+ *   gu       BF16 [rows, 2I], column groups [gate x8, up x8, ...]: output
+ *            column c takes gate = gu[r, 16*(c/8) + c%8] and
+ *            up = gu[r, 16*(c/8) + 8 + c%8]
+ *   clamp_L  the SwiGLU clamp L, finite, 0 < L <= 2^64
+ *   expert_offsets, num_experts
+ *            optional DEVICE int32 [num_experts + 1], non-decreasing; segment
+ *            e is rows [offsets[e], offsets[e+1]). When given, only rows in
+ *            [offsets[0], offsets[num_experts]) (clamped to [0, rows]) are
+ *            written and every other row of packed/sf is left untouched.
+ *            Pass NULL and 0 to process all rows. The offsets are read on
+ *            the device, so the call never synchronises and can be captured
+ *            in a CUDA graph with offsets that change between replays.
+ *   packed   uint8 [rows, I/2];  sf uint8 [rows, I/16]
+ */
+MOE_NVFP4_API int moe_swiglu_nvfp4_quantize(const uint16_t *gu, int64_t rows, int64_t I, float clamp_L,
+                              const int32_t *expert_offsets, int32_t num_experts,
+                              uint8_t *packed, uint8_t *sf, moe_nvfp4_stream_t stream);
+
+/*
+ * Diagnostic: the fp32 SwiGLU values y [rows, I] of the fused kernel's fast
+ * path (before its boundary re-evaluation), in output-column order. Used to
+ * measure the fast path's error against a double-precision evaluation.
+ * Same argument rules as moe_swiglu_nvfp4_quantize; y must be 16-byte
+ * aligned.
+ */
+MOE_NVFP4_API int moe_swiglu_fast_values(const uint16_t *gu, int64_t rows, int64_t I, float clamp_L,
+                           float *y, moe_nvfp4_stream_t stream);
+
+/*
+ * Diagnostic: as moe_swiglu_nvfp4_quantize, and also adds to the caller's
+ * DEVICE counters (uint64 [3], not cleared by the call):
+ *   [0] blocks processed, [1] blocks whose scale needed the re-evaluation,
+ *   [2] elements whose nibble needed the re-evaluation.
+ */
+MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_counted(const uint16_t *gu, int64_t rows, int64_t I,
+                                      float clamp_L, const int32_t *expert_offsets,
+                                      int32_t num_experts, uint8_t *packed, uint8_t *sf,
+                                      uint64_t *counters, moe_nvfp4_stream_t stream);
+
+/* The relative window the fused kernel uses for a clamp L: a scale or
+ * nibble decision whose fast-path input lies within this relative distance
+ * of a rounding boundary is redone from a double-precision SwiGLU value.
+ * It bounds the fast path's relative error (fp32 exponent-argument rounding,
+ * which grows with the most negative gate that can still reach a nonzero
+ * nibble for this L, plus the approximate exp2 and reciprocal), with a
+ * factor 2 of margin. Returns a negative value for an invalid L. */
+MOE_NVFP4_API double moe_swiglu_nvfp4_window(float clamp_L);
+
+/* Static text for a return code. */
+MOE_NVFP4_API const char *moe_nvfp4_strerror(int code);
+
+/* ABI version of this header (incremented on any signature change). */
+MOE_NVFP4_API int moe_nvfp4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,196 @@
+"""GB300 (sm_103a) MoE expert activation step: deinterleave + clamped SwiGLU
++ NVFP4 quantize, behind the C ABI of ``libmoe_swiglu_nvfp4.so``
+(``include/moe_nvfp4.h``).
+
+This module only marshals arguments: it checks torch tensors, takes their
+device pointers and the current CUDA stream, and calls the C entry point of
+the same name. Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback, and importing the binding fails
+loudly when the library has not been built (``python -m
+moe_swiglu_epilogue_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_values",
+           "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
+           "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
+
+_lib = None
+
+
+class MoeNvfp4Error(RuntimeError):
+    def __init__(self, code: int, name: str):
+        self.code = code
+        super().__init__(f"{name}: {moe_nvfp4_strerror(code)} (code {code})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m moe_swiglu_epilogue_gb300.build` (no fallback exists)")
+    lib = ctypes.CDLL(path)
+    P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    lib.moe_nvfp4_quantize.argtypes = [P, I64, I64, P, P, P]
+    lib.moe_nvfp4_quantize.restype = ctypes.c_int
+    lib.moe_swiglu_nvfp4_quantize.argtypes = [P, I64, I64, F, P, I32, P, P, P]
+    lib.moe_swiglu_nvfp4_quantize.restype = ctypes.c_int
+    lib.moe_swiglu_fast_values.argtypes = [P, I64, I64, F, P, P]
+    lib.moe_swiglu_fast_values.restype = ctypes.c_int
+    lib.moe_swiglu_nvfp4_quantize_counted.argtypes = [P, I64, I64, F, P, I32, P, P, P, P]
+    lib.moe_swiglu_nvfp4_quantize_counted.restype = ctypes.c_int
+    lib.moe_swiglu_nvfp4_window.argtypes = [F]
+    lib.moe_swiglu_nvfp4_window.restype = ctypes.c_double
+    lib.moe_nvfp4_strerror.argtypes = [ctypes.c_int]
+    lib.moe_nvfp4_strerror.restype = ctypes.c_char_p
+    lib.moe_nvfp4_abi_version.argtypes = []
+    lib.moe_nvfp4_abi_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def moe_nvfp4_strerror(code: int) -> str:
+    return load_library().moe_nvfp4_strerror(int(code)).decode()
+
+
+def moe_swiglu_nvfp4_window(clamp_L: float) -> float:
+    return float(load_library().moe_swiglu_nvfp4_window(float(clamp_L)))
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor front end
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _bf16_bits(t, name: str, width_mult: int):
+    torch = _torch()
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (torch.bfloat16, torch.uint16, torch.int16):
+        raise ValueError(f"{name} must hold BF16 (bfloat16, or its bits as uint16/int16)")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    if t.shape[1] % width_mult:
+        raise ValueError(f"{name}.shape[1] must be a multiple of {width_mult}")
+    return t
+
+
+def _out(t, shape, device, name: str):
+    torch = _torch()
+    if t is None:
+        return torch.empty(shape, dtype=torch.uint8, device=device)
+    if t.dtype != torch.uint8 or tuple(t.shape) != tuple(shape) or not t.is_contiguous() \
+            or t.device != device:
+        raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor of shape {shape}")
+    return t
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise MoeNvfp4Error(rc, name)
+
+
+def moe_nvfp4_quantize(x, packed=None, sf=None, stream=None):
+    """Quantize-only: x BF16 [rows, K] -> (packed uint8 [rows, K/2],
+    sf uint8 [rows, K/16]; view sf as torch.float8_e4m3fn for the values)."""
+    x = _bf16_bits(x, "x", 16)
+    rows, K = x.shape
+    packed = _out(packed, (rows, K // 2), x.device, "packed")
+    sf = _out(sf, (rows, K // 16), x.device, "sf")
+    with _torch().cuda.device(x.device):
+        rc = load_library().moe_nvfp4_quantize(
+            ctypes.c_void_p(x.data_ptr()), rows, K, ctypes.c_void_p(packed.data_ptr()),
+            ctypes.c_void_p(sf.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_nvfp4_quantize")
+    return packed, sf
+
+
+def _offsets_arg(offsets, device):
+    torch = _torch()
+    if offsets is None:
+        return ctypes.c_void_p(0), 0
+    if not offsets.is_cuda or offsets.dtype != torch.int32 or offsets.dim() != 1 \
+            or not offsets.is_contiguous() or offsets.device != device:
+        raise ValueError("expert_offsets must be a contiguous int32 CUDA tensor [E+1] "
+                         "on the input's device")
+    return ctypes.c_void_p(offsets.data_ptr()), offsets.shape[0] - 1
+
+
+def moe_swiglu_nvfp4_quantize(gu, clamp_L: float, expert_offsets=None, packed=None, sf=None,
+                              stream=None):
+    """Fused: gu BF16 [rows, 2I] in [gate x8, up x8, ...] groups ->
+    (packed uint8 [rows, I/2], sf uint8 [rows, I/16]). With expert_offsets
+    (int32 [E+1] on the device) rows outside [offsets[0], offsets[E]) are
+    left untouched; pass preallocated `packed`/`sf` to keep them."""
+    gu = _bf16_bits(gu, "gu", 32)
+    rows, two_i = gu.shape
+    I = two_i // 2
+    packed = _out(packed, (rows, I // 2), gu.device, "packed")
+    sf = _out(sf, (rows, I // 16), gu.device, "sf")
+    off_p, E = _offsets_arg(expert_offsets, gu.device)
+    with _torch().cuda.device(gu.device):
+        rc = load_library().moe_swiglu_nvfp4_quantize(
+            ctypes.c_void_p(gu.data_ptr()), rows, I, float(clamp_L), off_p, E,
+            ctypes.c_void_p(packed.data_ptr()), ctypes.c_void_p(sf.data_ptr()),
+            _stream_ptr(stream))
+    _check(rc, "moe_swiglu_nvfp4_quantize")
+    return packed, sf
+
+
+def moe_swiglu_nvfp4_quantize_counted(gu, clamp_L: float, counters, expert_offsets=None,
+                                      packed=None, sf=None, stream=None):
+    """As moe_swiglu_nvfp4_quantize, adding to `counters` (int64 CUDA [3]):
+    blocks processed, scale re-evaluations, nibble re-evaluations."""
+    torch = _torch()
+    gu = _bf16_bits(gu, "gu", 32)
+    rows, two_i = gu.shape
+    I = two_i // 2
+    if counters.dtype != torch.int64 or counters.numel() != 3 or not counters.is_cuda:
+        raise ValueError("counters must be an int64 CUDA tensor of 3 elements")
+    packed = _out(packed, (rows, I // 2), gu.device, "packed")
+    sf = _out(sf, (rows, I // 16), gu.device, "sf")
+    off_p, E = _offsets_arg(expert_offsets, gu.device)
+    with torch.cuda.device(gu.device):
+        rc = load_library().moe_swiglu_nvfp4_quantize_counted(
+            ctypes.c_void_p(gu.data_ptr()), rows, I, float(clamp_L), off_p, E,
+            ctypes.c_void_p(packed.data_ptr()), ctypes.c_void_p(sf.data_ptr()),
+            ctypes.c_void_p(counters.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_swiglu_nvfp4_quantize_counted")
+    return packed, sf
+
+
+def moe_swiglu_fast_values(gu, clamp_L: float, stream=None):
+    """Diagnostic: the fused kernel's fast-path fp32 SwiGLU values [rows, I]."""
+    torch = _torch()
+    gu = _bf16_bits(gu, "gu", 32)
+    rows, two_i = gu.shape
+    y = torch.empty((rows, two_i // 2), dtype=torch.float32, device=gu.device)
+    with torch.cuda.device(gu.device):
+        rc = load_library().moe_swiglu_fast_values(
+            ctypes.c_void_p(gu.data_ptr()), rows, two_i // 2, float(clamp_L),
+            ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_swiglu_fast_values")
+    return y

@@ -1,0 +1,194 @@
+"""Test helpers: comparing kernel outputs with the oracle, and building
+adversarial inputs by searching the oracle. Uses only the oracle, numpy and
+the seeded workload generators -- never the CUDA path."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+import oracle
+from moe_swiglu_epilogue_gb300 import workloads as W
+
+# Fused-path tolerance: scale bytes exact; a nibble may differ by one E2M1
+# step, on at most 1e-5 of the elements, and only where a fp32 SwiGLU value
+# within 2 ulp of the oracle's would have produced the kernel's nibble.
+MAX_NIBBLE_MISMATCH_FRACTION = 1e-5
+MAX_ULPS = 2
+
+
+def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
+    """[..., n/2] bytes -> [..., n] nibbles (even element = low nibble)."""
+    p = np.asarray(packed, np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = p & 0x0F
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def signed_index(nib: np.ndarray) -> np.ndarray:
+    idx = (nib & 7).astype(np.int32)
+    return np.where(nib & 8, -idx, idx)
+
+
+@dataclass
+class FusedReport:
+    elements: int
+    sf_mismatches: int
+    nibble_mismatches: int
+    outside_tolerance: int
+
+    @property
+    def exact(self) -> bool:
+        return self.sf_mismatches == 0 and self.nibble_mismatches == 0
+
+    def assert_within_tolerance(self):
+        assert self.sf_mismatches == 0, self
+        assert self.nibble_mismatches <= MAX_NIBBLE_MISMATCH_FRACTION * self.elements, self
+        assert self.outside_tolerance == 0, self
+
+
+def _ulp_neighbours(y: float, k: int):
+    v = np.float32(y)
+    out = []
+    up, dn = v, v
+    for _ in range(k):
+        up = np.nextafter(up, np.float32(np.inf))
+        dn = np.nextafter(dn, np.float32(-np.inf))
+        out += [up, dn]
+    return out
+
+
+def compare_fused(gpu_packed, gpu_sf, ref_packed, ref_sf, y_oracle_at) -> FusedReport:
+    """gpu_* / ref_*: packed [n, I/2] and sf [n, I/16] for the same n rows or
+    blocks. y_oracle_at(row, col) gives the oracle's fp32 SwiGLU value there
+    (only called for mismatching nibbles)."""
+    gpu_sf = np.asarray(gpu_sf); ref_sf = np.asarray(ref_sf)
+    sf_bad = int(np.count_nonzero(gpu_sf != ref_sf))
+    gn = unpack_nibbles(gpu_packed); rn = unpack_nibbles(ref_packed)
+    bad = np.argwhere(gn != rn)
+    outside = 0
+    for r, c in bad:
+        g, o = int(gn[r, c]), int(rn[r, c])
+        if abs(int(signed_index(np.uint8(g))) - int(signed_index(np.uint8(o)))) > 1:
+            outside += 1
+            continue
+        y = y_oracle_at(int(r), int(c))
+        code = int(ref_sf[r, c // 16])
+        if not any(oracle.quantize_element_with_scale(float(v), code) == g
+                   for v in _ulp_neighbours(y, MAX_ULPS)):
+            outside += 1
+    return FusedReport(int(gn.size), sf_bad, int(bad.shape[0]), outside)
+
+
+# ---------------------------------------------------------------------------
+# Adversarial blocks
+# ---------------------------------------------------------------------------
+
+def e4m3_value(code: int) -> float:
+    return oracle.fp8_e4m3_to_float32(code)
+
+
+def quantize_edge_blocks(rng, n_blocks: int) -> np.ndarray:
+    """BF16 quantize-only blocks [n, 16] (uint16) built around exact
+    boundaries: the block amax on 6 x E4M3 values and on 6 x the midpoints
+    between neighbours (scale ties, including the subnormal ones and the
+    underflow tie 6 * 2^-10), elements on half-step ties (2k+1)/4 * d and
+    their BF16 neighbours, +-0, and saturating blocks (amax 6 * 448 and far
+    beyond). Values that BF16 cannot hold exactly round to a neighbour."""
+    blocks = []
+    codes = list(range(1, 0x7f))
+    for n in range(n_blocks):
+        kind = n % 6
+        c = codes[rng.integers(len(codes))]
+        d = e4m3_value(c)
+        y = np.zeros(16, np.float64)
+        if kind in (0, 1):                      # half-step ties under scale d
+            y[0] = 6 * d
+            k = rng.integers(0, 12, 15)
+            y[1:] = (2 * k + 1) / 4 * d
+        elif kind == 2:                         # scale tie: amax = 6 * midpoint
+            c2 = min(c + 1, 0x7e)
+            y[0] = 3 * (d + e4m3_value(c2))
+            y[1:] = rng.uniform(-1, 1, 15) * y[0]
+        elif kind == 3:                         # subnormal scales and their ties
+            m = rng.integers(1, 9)
+            y[0] = 6 * (m + (0.5 if rng.integers(2) else 0.0)) * 2.0 ** -9
+            y[1:] = rng.uniform(-1, 1, 15) * y[0]
+        elif kind == 4:                         # saturation
+            y[0] = [6 * 448.0, 6 * 464.0, 6 * 480.0, 1e5, 3e38][rng.integers(5)]
+            y[1:] = rng.uniform(-1, 1, 15) * y[0]
+        else:                                   # signed zeros and tiny values
+            y[:] = rng.choice([0.0, -0.0, 1e-40, -1e-40, 6 * 2.0 ** -10, -6 * 2.0 ** -11], 16)
+        y *= np.where(rng.integers(0, 2, 16) == 1, -1.0, 1.0)
+        perm = rng.permutation(16)
+        bits = W.bf16_bits(y.astype(np.float32))
+        # keep exact ties exact: when the fp32 -> bf16 rounding moved a value,
+        # also try the truncated neighbour at random
+        trunc = (y.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        pick = rng.integers(0, 2, 16) == 1
+        bits = np.where(pick, trunc, bits)
+        blocks.append(bits[perm])
+    return np.stack(blocks)
+
+
+def fused_near_tie_blocks(rng, n_blocks: int, L: float, gate_lo: float = -6.0):
+    """Interleaved BF16 blocks [n, 32] whose oracle SwiGLU values land as
+    close as BF16 (gate, up) pairs allow to rounding boundaries: the block
+    amax on 6 x an E4M3 value, or on 6 x the midpoint between two (a scale
+    tie, subnormal scales included), the other 15 outputs on half-step ties
+    (2k+1)/4 * d. For every target, every BF16 gate in [gate_lo, L + 1] is
+    paired with the two BF16 ups around target / silu(gate), and the pair
+    whose oracle value is nearest wins. Exact hits are rare (a BF16 up has
+    8 bits, so a gate lands within half an fp32 ulp of a target with
+    probability ~2^-16); most values end a few ulps from their boundary.
+    Returns (blocks, {"exact_hits", "median_rel_distance", "targets"})."""
+    allg = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    gf = W.bf16_to_f32(allg)
+    sel = np.isfinite(gf) & (gf >= gate_lo) & (gf <= L + 1.0)
+    gf = gf[sel]
+    sig = oracle.swiglu_clamped_array(gf, np.ones_like(gf), L).astype(np.float64)
+    keep = np.abs(sig) >= 2.0 ** -6
+    gf, sig = gf[keep], sig[keep]
+
+    targets = np.zeros((n_blocks, 16))
+    for n in range(n_blocks):
+        code = int(rng.integers(1, 0x48))         # scales up to 3.75: |y| <= L silu(L)
+        d = e4m3_value(code)
+        amax = 3 * (d + e4m3_value(code + 1)) if n % 3 == 0 else 6 * d
+        targets[n, 0] = amax
+        targets[n, 1:] = (2 * rng.integers(0, 12, 15) + 1) / 4 * d
+    targets *= np.where(rng.integers(0, 2, targets.shape) == 1, -1.0, 1.0)
+    flat = targets.ravel()
+    best_g = np.zeros(flat.size, np.float32)
+    best_u = np.zeros(flat.size, np.float32)
+    hits = 0
+    rel_dist = np.zeros(flat.size)
+    for c0 in range(0, flat.size, 256):
+        t = flat[c0:c0 + 256]
+        ustar = t[:, None] / sig[None, :]
+        ok = np.abs(ustar) <= L
+        ub = (np.where(ok, ustar, 0.0).astype(np.float32).view(np.uint32) >> 16)
+        G = np.broadcast_to(gf[None, :], ustar.shape)
+        best_d = np.full(t.size, np.inf)
+        for delta in (0, 1):
+            U = W.bf16_to_f32((ub + delta).astype(np.uint16))
+            y = oracle.swiglu_clamped_array(G, U, L).reshape(ustar.shape).astype(np.float64)
+            dist = np.where(ok, np.abs(y - t[:, None]), np.inf)
+            j = np.argmin(dist, axis=1)
+            dj = dist[np.arange(t.size), j]
+            better = dj < best_d
+            best_d = np.where(better, dj, best_d)
+            rows = np.nonzero(better)[0]
+            best_g[c0 + rows] = gf[j[rows]]
+            best_u[c0 + rows] = U[rows, j[rows]]
+        hits += int(np.count_nonzero(best_d == 0))
+        rel_dist[c0:c0 + t.size] = best_d / np.abs(t)
+    out = np.zeros((n_blocks, 32), np.uint16)
+    for n in range(n_blocks):
+        perm = rng.permutation(16)
+        gate = W.bf16_bits(best_g[16 * n:16 * n + 16][perm])
+        up = W.bf16_bits(best_u[16 * n:16 * n + 16][perm])
+        out[n] = W.interleave_gate_up(gate[None, :], up[None, :])[0]
+    return out, {"exact_hits": hits, "median_rel_distance": float(np.median(rel_dist)),
+                 "targets": int(flat.size)}

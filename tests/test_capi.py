@@ -1,0 +1,94 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/moe_nvfp4.h declares, and rejects bad arguments on the host
+before any CUDA call (none of these calls reach the device)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_swiglu_epilogue_gb300 import build, load_library
+    build.build()
+    return load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(
+        r"^\s*MOE_NVFP4_API\s+(?:const\s+)?[a-z_0-9]+\s*\*?\s*(moe_[a-z_0-9]+)\s*\(",
+        text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_nvfp4_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert [e for e in exported if e.startswith("moe_")] == declared_functions()
+
+
+def test_abi_version_and_strerror(lib):
+    assert lib.moe_nvfp4_abi_version() == 1
+    for code in range(0, -8, -1):
+        assert lib.moe_nvfp4_strerror(code)
+    assert b"unknown" in lib.moe_nvfp4_strerror(-99)
+
+
+# Fake device addresses with chosen alignment. Every call below must be
+# rejected on the host (or have rows == 0) so that nothing is ever launched
+# on them, even when this file runs on a machine with a GPU.
+A32 = ctypes.c_void_p(0x7f0000000000)
+A16 = ctypes.c_void_p(0x7f0000000010)
+A2 = ctypes.c_void_p(0x7f0000000002)
+NULL = ctypes.c_void_p(0)
+S = ctypes.c_void_p(0)
+
+
+def test_quantize_argument_errors(lib):
+    q = lib.moe_nvfp4_quantize
+    assert q(A32, -1, 32, A16, A16, S) == -4
+    assert q(A32, 4, 24, A16, A16, S) == -2
+    assert q(A32, 4, 0, A16, A16, S) == -2
+    assert q(NULL, 4, 32, A16, A16, S) == -1
+    assert q(A32, 4, 32, NULL, A16, S) == -1
+    assert q(A16, 4, 32, A16, A16, S) == -3       # input only 16-byte aligned
+    assert q(A32, 4, 32, A2, A16, S) == -3
+    assert q(A32, 2 ** 62, 2 ** 10, A16, A16, S) == -4
+    assert q(NULL, 0, 32, NULL, NULL, S) == 0     # nothing to do, nothing launched
+
+
+def test_fused_argument_errors(lib):
+    f = lib.moe_swiglu_nvfp4_quantize
+    for bad_L in (0.0, -1.0, float("nan"), float("inf"), 1e30):
+        assert f(A32, 0, 32, bad_L, NULL, 0, A16, A16, S) == -5
+    assert f(A32, 0, 32, 7.0, NULL, -1, A16, A16, S) == -6
+    assert f(A32, 0, 32, 7.0, NULL, 3, A16, A16, S) == -6
+    assert f(A32, 4, 40, 7.0, NULL, 0, A16, A16, S) == -2
+    assert f(A16, 4, 32, 7.0, NULL, 0, A16, A16, S) == -3
+    assert f(A32, 0, 32, 7.0, NULL, 0, A16, A16, S) == 0
+
+
+def test_window(lib):
+    w7 = lib.moe_swiglu_nvfp4_window(7.0)
+    w10 = lib.moe_swiglu_nvfp4_window(10.0)
+    assert 2 ** -20 < w7 < 2 ** -16
+    assert w7 <= w10 <= lib.moe_swiglu_nvfp4_window(1e6)
+    assert lib.moe_swiglu_nvfp4_window(-1.0) < 0
+    assert lib.moe_swiglu_nvfp4_window(float("nan")) < 0

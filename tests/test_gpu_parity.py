@@ -1,0 +1,322 @@
+"""Parity of the CUDA kernels with the oracle, through the C ABI.
+
+Quantize-only must be bit-exact. The fused path must meet the stated
+tolerance (scale bytes exact; a nibble may be one E2M1 step off on at most
+1e-5 of the elements, and only where a SwiGLU value within 2 ulp of the
+oracle's would give the kernel's nibble); the kernel is designed to be
+exact, and the tests also assert that.
+
+Small cases run the oracle on every element; full-size cases, in the same
+launch configuration the benchmark times, compare sampled blocks plus every
+block of the first and last active rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_swiglu_epilogue_gb300 as M
+from moe_swiglu_epilogue_gb300 import workloads as W
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from moe_swiglu_epilogue_gb300 import build
+    build.build()
+    oracle.build()
+    M.load_library()
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def run_quantize(x_bits):
+    p, s = M.moe_nvfp4_quantize(dev(x_bits))
+    torch.cuda.synchronize()
+    return p.cpu().numpy(), s.cpu().numpy()
+
+
+def run_fused(gu_bits, L, offsets=None, packed=None, sf=None):
+    off = None if offsets is None else torch.from_numpy(np.asarray(offsets, np.int32)).cuda()
+    p = None if packed is None else torch.from_numpy(packed.copy()).cuda()
+    s = None if sf is None else torch.from_numpy(sf.copy()).cuda()
+    p, s = M.moe_swiglu_nvfp4_quantize(dev(gu_bits), L, off, p, s)
+    torch.cuda.synchronize()
+    return p.cpu().numpy(), s.cpu().numpy()
+
+
+def check_fused_full(gu, L, gp, gs, rp, rs, exact=True):
+    rep = parity.compare_fused(gp, gs, rp, rs,
+                               lambda r, c: float(oracle.swiglu_values(gu, L, r, r + 1)[0, c]))
+    rep.assert_within_tolerance()
+    if exact:
+        assert rep.exact, rep
+    return rep
+
+
+# ---------------------------------------------------------------------------
+# quantize-only: bit-exact
+# ---------------------------------------------------------------------------
+
+def test_quantize_normal_workload_bit_exact():
+    w = W.quantize_normal()                               # x [128, 2048] ~ N(0,1), seed 0
+    gp, gs = run_quantize(w.data)
+    rp, rs = oracle.quantize_nvfp4(w.data)
+    assert np.array_equal(gs, rs) and np.array_equal(gp, rp)
+
+
+def test_quantize_heavy_tail_with_saturation_bit_exact():
+    w = W.prefill_heavy_tail_quantize(rows=2048, K=3072)
+    gp, gs = run_quantize(w.data)
+    rp, rs = oracle.quantize_nvfp4(w.data)
+    # all-zero blocks occur; saturation at 448 needs |t3| > 54 on an outlier,
+    # rare at this size (it is forced in the edge blocks and the element map)
+    assert np.any(rs == 0)
+    assert np.array_equal(gs, rs) and np.array_equal(gp, rp)
+
+
+def test_quantize_edge_blocks_bit_exact():
+    rng = np.random.default_rng(50)
+    blocks = parity.quantize_edge_blocks(rng, 24000)      # ties, saturation, zeros
+    x = blocks.reshape(-1, 16 * 16)
+    gp, gs = run_quantize(x)
+    rp, rs = oracle.quantize_nvfp4(x)
+    assert np.array_equal(gs, rs)
+    assert np.array_equal(gp, rp)
+
+
+def _element_map_input():
+    """Every finite BF16 value x under every scale code: for each code c a
+    leader element fixes sf = c (amax = 6 * value(c) exactly; for 0x7e the
+    largest BF16; for 0 the underflow tie 6 * 2^-10) and the other 15 slots
+    hold, in turn, every BF16 x with |x| <= the leader."""
+    allb = np.arange(0, 0x7F80, dtype=np.uint16)            # positive finite BF16
+    vals = W.bf16_to_f32(allb)
+    rows = []
+    for code in range(0, 0x7f):
+        if code == 0:
+            lead = np.float32(6 * 2.0 ** -10)
+        elif code == 0x7e:
+            lead = np.float32(W.bf16_to_f32(np.uint16(0x7F7F)))
+        else:
+            lead = np.float32(6 * oracle.fp8_e4m3_to_float32(code))
+        members = allb[vals <= lead]
+        members = np.concatenate([members, members | 0x8000])
+        pad = (-members.size) % 15
+        members = np.concatenate([members, np.zeros(pad, np.uint16)]).reshape(-1, 15)
+        lead_bits = W.bf16_bits(np.array([lead], np.float32))[0]
+        assert W.bf16_to_f32(lead_bits) == lead
+        blk = np.concatenate([np.full((members.shape[0], 1), lead_bits, np.uint16), members], 1)
+        rows.append(blk)
+    blocks = np.concatenate(rows)
+    pad = (-blocks.shape[0]) % 64
+    blocks = np.concatenate([blocks, np.zeros((pad, 16), np.uint16)])
+    return blocks.reshape(-1, 64 * 16)
+
+
+def test_quantize_exhaustive_element_map_bit_exact():
+    x = _element_map_input()
+    gp, gs = run_quantize(x)
+    rp, rs = oracle.quantize_nvfp4(x)
+    assert set(np.unique(rs)) >= set(range(0, 0x7f))      # every scale code occurs
+    assert np.array_equal(gs, rs)
+    assert np.array_equal(gp, rp)
+
+
+# ---------------------------------------------------------------------------
+# fused: small cases, every element checked
+# ---------------------------------------------------------------------------
+
+def test_fused_normal_workload():
+    w = W.fused_normal()                                  # [512, 2x2048], L = 7
+    gp, gs = run_fused(w.data, w.clamp_L)
+    rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L)
+    check_fused_full(w.data, w.clamp_L, gp, gs, rp, rs)
+
+
+def test_fused_ragged_segments_leave_other_rows_untouched():
+    w = W.ragged_routing(tokens=512, experts=32, topk=8, I=256, pad_rows=37)
+    rows, I = w.rows, w.width
+    for shift, offsets in [(0, w.offsets), (5, None)]:
+        if offsets is None:                   # segments starting after row 0, one empty
+            offsets = np.concatenate([[5, 5], w.offsets[2:-1] + 5, [rows - 3]]).astype(np.int32)
+            offsets = np.maximum.accumulate(offsets)
+        sent_p = np.full((rows, I // 2), 0xA5, np.uint8)
+        sent_s = np.full((rows, I // 16), 0x5A, np.uint8)
+        gp, gs = run_fused(w.data, w.clamp_L, offsets, sent_p, sent_s)
+        rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L, offsets,
+                                              packed=sent_p.copy(), sf=sent_s.copy())
+        r0, r1 = int(offsets[0]), int(offsets[-1])
+        assert np.all(gp[:r0] == 0xA5) and np.all(gp[r1:] == 0xA5)
+        assert np.all(gs[:r0] == 0x5A) and np.all(gs[r1:] == 0x5A)
+        check_fused_full(w.data, w.clamp_L, gp, gs, rp, rs)
+
+
+def test_fused_offsets_outside_the_buffer_are_clamped():
+    w = W.fused_normal(rows=40, I=64)
+    offsets = np.array([-7, 10, 1000], np.int32)           # clamped to [0, 40)
+    gp, gs = run_fused(w.data, w.clamp_L, offsets)
+    rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L)
+    check_fused_full(w.data, w.clamp_L, gp, gs, rp, rs)
+
+
+def test_fused_prefill_heavy_tail():
+    w = W.prefill_heavy_tail(rows=1024, I=3072)           # L = 10, outliers, zero blocks
+    gp, gs = run_fused(w.data, w.clamp_L)
+    rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L)
+    assert np.any(rs == 0)
+    check_fused_full(w.data, w.clamp_L, gp, gs, rp, rs)
+
+
+def test_fused_edge_with_near_tie_blocks():
+    w = W.edge_structured(rows=512, I=4096)
+    gu = w.data.copy()
+    kinds = w.meta["kinds"]
+    struct = np.argwhere(kinds == W.EDGE_KINDS.index("structured") + 1)
+    rng = np.random.default_rng(77)
+    blocks, stats = parity.fused_near_tie_blocks(rng, struct.shape[0], w.clamp_L)
+    for (r, b), blk in zip(struct, blocks):
+        gu[r, 32 * b:32 * b + 32] = blk
+    gp, gs = run_fused(gu, w.clamp_L)
+    rp, rs = oracle.swiglu_quantize_nvfp4(gu, w.clamp_L)
+    # the constructed values sit inside the kernel's re-evaluation window
+    assert stats["median_rel_distance"] < M.moe_swiglu_nvfp4_window(w.clamp_L), stats
+    print(f"\nnear-tie blocks: {stats}")
+    assert np.any((rs > 0) & (rs < 8))                    # subnormal scales occur
+    check_fused_full(gu, w.clamp_L, gp, gs, rp, rs)
+
+
+@pytest.mark.parametrize("rows,I", [(1, 16), (37, 48), (3, 2048), (257, 4096), (5, 8192)])
+def test_fused_shapes_and_ragged_tails(rows, I):
+    w = W.fused_normal(rows=rows, I=I, seed=rows)
+    gp, gs = run_fused(w.data, w.clamp_L)
+    rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L)
+    check_fused_full(w.data, w.clamp_L, gp, gs, rp, rs)
+
+
+def test_zero_rows_is_a_no_op():
+    gu = torch.zeros((0, 64), dtype=torch.int16, device="cuda")
+    p, s = M.moe_swiglu_nvfp4_quantize(gu, 7.0)
+    x = torch.zeros((0, 32), dtype=torch.int16, device="cuda")
+    q, t = M.moe_nvfp4_quantize(x)
+    torch.cuda.synchronize()
+    assert p.shape == (0, 16) and s.shape == (0, 2) and q.shape == (0, 16) and t.shape == (0, 2)
+
+
+def test_fast_path_error_is_inside_half_the_window():
+    """The window doubles an analytic error bound of the fast path; the
+    measured error over every BF16 gate (with up = 1 and up = L) must stay
+    inside that bound."""
+    gates = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    gf = W.bf16_to_f32(gates)
+    finite = np.isfinite(gf)
+    gates, gf = gates[finite], gf[finite]
+    for L in (7.0, 10.0):
+        win = M.moe_swiglu_nvfp4_window(L)
+        worst = 0.0
+        for uval in (1.0, L, -L / 3):
+            up = W.bf16_bits(np.full(gates.shape, uval, np.float32))
+            n = gates.size - gates.size % 16
+            gu = W.interleave_gate_up(gates[:n].reshape(-1, 16), up[:n].reshape(-1, 16))
+            y_fast = M.moe_swiglu_fast_values(dev(gu), L).cpu().numpy().ravel()
+            y_ref = oracle.swiglu_values(gu, L).ravel()
+            big = np.abs(y_ref) >= 2.0 ** -12
+            rel = np.abs(y_fast[big].astype(np.float64) - y_ref[big]) / np.abs(y_ref[big])
+            worst = max(worst, float(rel.max()))
+        assert worst <= win / 2, (L, worst, win)
+
+
+def test_side_stream_and_graph_replay_with_new_offsets():
+    w = W.ragged_routing(tokens=256, experts=8, topk=4, I=512, pad_rows=11)
+    gu = dev(w.data)
+    rows, I = w.rows, w.width
+    off = torch.from_numpy(w.offsets).cuda()
+    packed = torch.full((rows, I // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    sf = torch.full((rows, I // 16), 0x5A, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        M.moe_swiglu_nvfp4_quantize(gu, w.clamp_L, off, packed, sf)      # warm-up off graph
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            M.moe_swiglu_nvfp4_quantize(gu, w.clamp_L, off, packed, sf)
+    torch.cuda.current_stream().wait_stream(s)
+    for new in (w.offsets, np.array([3, 40, 41, rows - 20, rows - 20, rows - 20, rows - 20,
+                                     rows - 20, rows - 20], np.int32)):
+        packed.fill_(0xA5); sf.fill_(0x5A)
+        off.copy_(torch.from_numpy(np.asarray(new, np.int32)))
+        g.replay()
+        torch.cuda.synchronize()
+        sent_p = np.full((rows, I // 2), 0xA5, np.uint8)
+        sent_s = np.full((rows, I // 16), 0x5A, np.uint8)
+        rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L, new, packed=sent_p, sf=sent_s)
+        assert np.array_equal(packed.cpu().numpy(), rp) and np.array_equal(sf.cpu().numpy(), rs)
+
+
+def test_counted_variant_matches_and_counts():
+    w = W.fused_normal(rows=512, I=2048)
+    counters = torch.zeros(3, dtype=torch.int64, device="cuda")
+    p1, s1 = M.moe_swiglu_nvfp4_quantize_counted(dev(w.data), w.clamp_L, counters)
+    p2, s2 = M.moe_swiglu_nvfp4_quantize(dev(w.data), w.clamp_L)
+    torch.cuda.synchronize()
+    c = counters.cpu().numpy()
+    assert torch.equal(p1, p2) and torch.equal(s1, s2)
+    assert c[0] == 512 * 2048 // 16
+    assert c[1] < 1e-3 * c[0] and c[2] < 1e-3 * 16 * c[0]
+    print(f"\nre-evaluated: {c[1]} of {c[0]} scales, {c[2]} of {16 * c[0]} nibbles")
+
+
+def test_repeat_runs_are_identical():
+    w = W.prefill_heavy_tail(rows=256, I=3072)
+    a = run_fused(w.data, w.clamp_L)
+    b = run_fused(w.data, w.clamp_L)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, as the benchmark launches them: sampled blocks
+# ---------------------------------------------------------------------------
+
+def _sampled_check(w, gp, gs, n_sample=60000, seed=0):
+    rng = np.random.default_rng(seed)
+    nb = w.width // 16
+    r0 = 0 if w.offsets is None else int(w.offsets[0])
+    r1 = w.rows if w.offsets is None else int(w.offsets[-1])
+    rows = rng.integers(r0, r1, n_sample)
+    blks = rng.integers(0, nb, n_sample)
+    edge_rows = np.repeat([r0, r1 - 1], nb)
+    rows = np.concatenate([rows, edge_rows])
+    blks = np.concatenate([blks, np.tile(np.arange(nb), 2)])
+    if w.kind == "quantize":
+        rp, rs = oracle.quantize_nvfp4_blocks(w.data, rows, blks)
+        gpb = gp.reshape(w.rows, nb, 8)[rows, blks]
+        assert np.array_equal(gs[rows, blks], rs) and np.array_equal(gpb, rp)
+        return
+    rp, rs = oracle.swiglu_quantize_nvfp4_blocks(w.data, w.clamp_L, rows, blks)
+    gpb = gp.reshape(w.rows, nb, 8)[rows, blks]
+    gsb = gs[rows, blks][:, None]
+
+    def y_at(k, c):
+        r, b = int(rows[k]), int(blks[k])
+        return float(oracle.swiglu_values(w.data[r:r + 1], w.clamp_L)[0, 16 * b + c])
+
+    rep = parity.compare_fused(gpb, gsb, rp, rs[:, None], y_at)
+    rep.assert_within_tolerance()
+    assert rep.exact, rep
+
+
+@pytest.mark.parametrize("name", ["ragged", "prefill", "edge", "prefill_quantize"])
+def test_full_size_workloads_sampled(name):
+    w = W.make(name)
+    if w.kind == "quantize":
+        gp, gs = run_quantize(w.data)
+    else:
+        gp, gs = run_fused(w.data, w.clamp_L, w.offsets)
+    assert not np.any(gs == 0x7f)
+    _sampled_check(w, gp, gs)
