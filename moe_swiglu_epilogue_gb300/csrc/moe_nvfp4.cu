@@ -38,6 +38,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "moe_nvfp4.h"
@@ -45,8 +46,14 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;                 // blocks in flight per thread
+constexpr int kUnroll = 2;                 // blocks in flight per lane
+constexpr int kMinBlocksFused = 3;         // resident CTAs per SM the register budget targets
+constexpr int kMinBlocksQuant = 4;
 constexpr int kMaxDevices = 64;
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr float kHalfStepBias = 6291456.0f;        // 1.5 * 2^22: fp32 spacing 0.5 there
+constexpr float kNegLog2e = -1.44269504088896341f;
+constexpr float kInv6 = 0.16666667163372039794921875f;   // RN(1/6)
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -78,6 +85,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Two fp32 -> two E4M3 codes, RNE, saturating: `hi` in bits 8-15, `lo` in 0-7.
 __device__ __forceinline__ uint32_t e4m3x2_rn_sat(float hi, float lo) {
     uint16_t r;
@@ -92,8 +117,8 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
     return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
 }
 
-// Eight signed half steps (exact multiples of 0.5 in [-6, 6]) -> eight E2M1
-// nibbles, element 0 in the low nibble of the low byte.
+// Eight signed half steps (exact multiples of 0.5; magnitudes above 6
+// saturate to 6) -> eight E2M1 nibbles, element 0 in the low nibble.
 __device__ __forceinline__ uint32_t e2m1x8(const float* v) {
     uint32_t r;
     asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
@@ -114,21 +139,32 @@ __device__ __forceinline__ uint32_t e2m1x8(const float* v) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Nearest multiple of 0.5 to t in [0, 6], ties to an even multiple: at
-// 1.5 * 2^22 the fp32 spacing is 0.5, so the add rounds t exactly so.
-__device__ __forceinline__ float round_half_step(float t) {
-    return __fadd_rn(__fadd_rn(t, 6291456.0f), -6291456.0f);
-}
-
 __device__ __forceinline__ float with_sign_of(float mag, float s) {
     return __uint_as_float(__float_as_uint(mag) | (__float_as_uint(s) & 0x80000000u));
 }
 
-// silu(min(g, L)) * clamp(u, -L, L) in fast fp32.
-__device__ __forceinline__ float swiglu_fast(float g, float u, float L) {
-    const float a = fminf(g, L);
-    const float b = fminf(fmaxf(u, -L), L);
-    const float e = ex2_approx(a * -1.44269504088896341f);   // exp(-a)
+// max |v_i| over 16 values, as a tree of 3-input maxima.
+__device__ __forceinline__ float abs_max16(const float* v) {
+    const float m0 = max3(fabsf(v[0]), fabsf(v[1]), fabsf(v[2]));
+    const float m1 = max3(fabsf(v[3]), fabsf(v[4]), fabsf(v[5]));
+    const float m2 = max3(fabsf(v[6]), fabsf(v[7]), fabsf(v[8]));
+    const float m3 = max3(fabsf(v[9]), fabsf(v[10]), fabsf(v[11]));
+    const float m4 = max3(fabsf(v[12]), fabsf(v[13]), fabsf(v[14]));
+    return max3(max3(m0, m1, m2), max3(m3, m4, fabsf(v[15])), 0.0f);
+}
+
+// a / 6, correctly rounded: q0 = a * RN(1/6) is within an ulp, the residual
+// a - 6 q0 is exact in one fma, and one correction step rounds correctly
+// (Markstein's theorem for a reciprocal rounded to nearest).
+__device__ __forceinline__ float div6(float a) {
+    const float q0 = a * kInv6;
+    const float r = fmaf(-q0, 6.0f, a);
+    return fmaf(r, kInv6, q0);
+}
+
+// silu(a) * b in fast fp32; a, b already clamped.
+__device__ __forceinline__ float silu_times_fast(float a, float b) {
+    const float e = ex2_approx(a * kNegLog2e);   // exp(-a)
     const float r = rcp_approx(1.0f + e);
     return (a * r) * b;
 }
@@ -158,6 +194,11 @@ __device__ __forceinline__ uint32_t nibble_by_definition(float y, float d, uint3
     return idx | ((__float_as_uint(s) >> 28) & 8u);
 }
 
+// Half-step index pairs (k, k+1) whose table entries differ, as a bit mask
+// over k: 0-1, 1-2, 2-3, 3-4, 5-6, 6-7, 10-11. A value near the boundary
+// between any other pair gets the same nibble on both sides.
+constexpr uint32_t kNibbleChangingBoundaries = 0x46Fu;
+
 // ---------------------------------------------------------------------------
 // Fused deinterleave + clamped SwiGLU + NVFP4 quantize
 // ---------------------------------------------------------------------------
@@ -167,13 +208,20 @@ struct FusedArgs {
     int64_t rows;
     int64_t bpr;               // blocks per row = I / 16
     float L;
+    uint32_t L2, negL2;        // (L, L) and (-L, -L) as BF16x2 (when L is a BF16 value)
     float W;                   // relative decision window
+    float Wp1, Wm1;            // 1 + W, 1 - W
+    float near_thr;            // 0.25 (1 - W)
     const int32_t* offsets;    // [E+1] or null
     int E;
     uint8_t* packed;           // [rows, I/2]
     uint8_t* sf;               // [rows, I/16]
     unsigned long long* counters;   // [3] or null (counted variant)
     float* values;             // [rows, I] (fast-values variant)
+};
+
+struct Tally {
+    unsigned long long blocks = 0, scales = 0, nibbles = 0;
 };
 
 __device__ __forceinline__ void active_block_range(const int32_t* offsets, int E, int64_t rows,
@@ -188,111 +236,161 @@ __device__ __forceinline__ void active_block_range(const int32_t* offsets, int E
     b1 = r1 * bpr;
 }
 
-template <bool kCount, bool kValues>
-__device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, const uint32_t* w,
-                                            unsigned long long& n_scale,
-                                            unsigned long long& n_elem) {
-    const float L = A.L, W = A.W;
-    float y[16];
-    float amax = 0.0f;
+// Scale code of a block whose fast amax lies within the window of an E4M3
+// rounding boundary: every element that could be the true maximum is
+// re-evaluated in double precision (and replaced in y), then the code is
+// taken from the exact amax.
+__device__ __forceinline__ uint32_t scale_by_definition(const uint16_t* blk_in, float L, float W,
+                                                        float amax, float* y) {
+    const float lim = amax * (1.0f - 2.0f * W);
+    float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-        const int grp = i >> 3, j = i & 7;
-        const uint32_t gw = w[8 * grp + (j >> 1)], uw = w[8 * grp + 4 + (j >> 1)];
-        const float g = (j & 1) ? bf16_hi(gw) : bf16_lo(gw);
-        const float u = (j & 1) ? bf16_hi(uw) : bf16_lo(uw);
-        y[i] = swiglu_fast(g, u, L);
-        amax = fmaxf(amax, fabsf(y[i]));
+        if (fabsf(y[i]) >= lim) {
+            float g, u;
+            gate_up_at(blk_in, i, g, u);
+            y[i] = swiglu_double(g, u, L);
+        }
+        am = fmaxf(am, fabsf(y[i]));
+    }
+    return e4m3x2_rn_sat(0.0f, __fdiv_rn(am, 6.0f)) & 0xFFu;
+}
+
+// Every lane of the warp calls this together (uniform control flow), with
+// `valid` false for lanes past the end of the stream.
+template <bool kCount, bool kValues, bool kBf16Clamp>
+__device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, bool valid,
+                                            const uint32_t* w, Tally& tally) {
+    const float L = A.L;
+    float y[16];
+#pragma unroll
+    for (int grp = 0; grp < 2; grp++) {
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            uint32_t gw = w[8 * grp + p], uw = w[8 * grp + 4 + p];
+            float g0, g1, u0, u1;
+            if (kBf16Clamp) {                        // clamp two values per instruction
+                gw = bf16x2_min(gw, A.L2);
+                uw = bf16x2_min(bf16x2_max(uw, A.negL2), A.L2);
+                g0 = bf16_lo(gw); g1 = bf16_hi(gw);
+                u0 = bf16_lo(uw); u1 = bf16_hi(uw);
+            } else {
+                g0 = fminf(bf16_lo(gw), L); g1 = fminf(bf16_hi(gw), L);
+                u0 = fminf(fmaxf(bf16_lo(uw), -L), L); u1 = fminf(fmaxf(bf16_hi(uw), -L), L);
+            }
+            y[8 * grp + 2 * p] = silu_times_fast(g0, u0);
+            y[8 * grp + 2 * p + 1] = silu_times_fast(g1, u1);
+        }
     }
     if (kValues) {
-        float4* out = reinterpret_cast<float4*>(A.values + blk * 16);
+        if (valid) {
+            float4* out = reinterpret_cast<float4*>(A.values + blk * 16);
 #pragma unroll
-        for (int k = 0; k < 4; k++) out[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+            for (int k = 0; k < 4; k++)
+                out[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+        }
         return;
     }
     const uint16_t* blk_in = A.gu + blk * 32;
 
     // scale: safe when both ends of the window round to the same code
-    const float q = __fdiv_rn(amax, 6.0f);
-    const uint32_t ends = e4m3x2_rn_sat(q * (1.0f + W), q * (1.0f - W));
+    const float amax = abs_max16(y);
+    const float q = div6(amax);
+    const uint32_t ends = e4m3x2_rn_sat(q * A.Wp1, q * A.Wm1);
     uint32_t code = ends & 0xFFu;
-    if ((ends >> 8) != code) {
-        // re-evaluate every element that could be the true maximum
-        const float lim = amax * (1.0f - 2.0f * W);
-        float am = 0.0f;
-        for (int i = 0; i < 16; i++) {
-            if (fabsf(y[i]) >= lim) {
-                float g, u;
-                gate_up_at(blk_in, i, g, u);
-                y[i] = swiglu_double(g, u, L);
-            }
-            am = fmaxf(am, fabsf(y[i]));
-        }
-        code = e4m3x2_rn_sat(0.0f, __fdiv_rn(am, 6.0f)) & 0xFFu;
-        if (kCount) n_scale++;
+    if (valid && (ends >> 8) != code) {
+        code = scale_by_definition(blk_in, L, A.W, amax, y);
+        if (kCount) tally.scales++;
     }
 
+    // nibbles: half step of t = |y| / d by one fma against the bias; the
+    // block's closeness max_i(|t_i - h_i| + W h_i) flags any t within the
+    // window of a half-step boundary
     const float d = e4m3_value(code);
     const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
-    float hs[16];
-    uint32_t near = 0;
+    float hs[16], cl[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-        const float t = fminf(fabsf(y[i]) * inv, 6.0f);
-        const float h = round_half_step(t);
-        near |= (fmaf(W, t, fabsf(t - h)) > 0.25f ? 1u : 0u) << i;
+        const float ay = fabsf(y[i]);
+        const float h = fmaf(ay, inv, kHalfStepBias) - kHalfStepBias;
+        cl[i] = fmaf(A.W, h, fabsf(fmaf(ay, inv, -h)));
         hs[i] = with_sign_of(h, y[i]);
     }
+    const float closeness = abs_max16(cl);
     uint32_t lo = e2m1x8(hs), hi = e2m1x8(hs + 8);
-    if (near != 0u) {
-        for (int i = 0; i < 16; i++) {
-            if (!((near >> i) & 1u)) continue;
-            float g, u;
-            gate_up_at(blk_in, i, g, u);
-            const uint32_t nib = nibble_by_definition(swiglu_double(g, u, L), d, code);
-            const int sh = 4 * (i & 7);
-            if (i < 8) lo = (lo & ~(0xFu << sh)) | (nib << sh);
-            else       hi = (hi & ~(0xFu << sh)) | (nib << sh);
-            if (kCount) n_elem++;
+
+    const bool near = valid && closeness > A.near_thr;
+    if (__any_sync(kFullMask, near)) {
+        uint32_t todo = 0;
+        if (near) {
+            for (int i = 0; i < 16; i++) {
+                const float ay = fabsf(y[i]);
+                const float h = fmaf(ay, inv, kHalfStepBias) - kHalfStepBias;
+                const float rr = fmaf(ay, inv, -h);
+                if (fmaf(A.W, h, fabsf(rr)) > A.near_thr) {
+                    // the boundary in question sits between half steps k and k+1
+                    const int k = __float2int_rn(2.0f * h) - (rr < 0.0f ? 1 : 0);
+                    if (k >= 0 && k < 12 && ((kNibbleChangingBoundaries >> k) & 1u)) todo |= 1u << i;
+                }
+            }
+        }
+        // one double-precision SwiGLU per lane per pass, all lanes together
+        while (__any_sync(kFullMask, todo != 0u)) {
+            if (todo != 0u) {
+                const int i = __ffs(todo) - 1;
+                todo &= todo - 1u;
+                float g, u;
+                gate_up_at(blk_in, i, g, u);
+                const uint32_t nib = nibble_by_definition(swiglu_double(g, u, L), d, code);
+                const int sh = 4 * (i & 7);
+                if (i < 8) lo = (lo & ~(0xFu << sh)) | (nib << sh);
+                else       hi = (hi & ~(0xFu << sh)) | (nib << sh);
+                if (kCount) tally.nibbles++;
+            }
         }
     }
-    *reinterpret_cast<uint2*>(A.packed + blk * 8) = make_uint2(lo, hi);
-    A.sf[blk] = static_cast<uint8_t>(code);
+    if (valid) {
+        *reinterpret_cast<uint2*>(A.packed + blk * 8) = make_uint2(lo, hi);
+        A.sf[blk] = static_cast<uint8_t>(code);
+        if (kCount) tally.blocks++;
+    }
 }
 
-template <bool kCount, bool kValues>
-__global__ void __launch_bounds__(kThreads)
+template <bool kCount, bool kValues, bool kBf16Clamp>
+__global__ void __launch_bounds__(kThreads, kMinBlocksFused)
 swiglu_nvfp4_kernel(const FusedArgs A) {
     int64_t b0, b1;
     active_block_range(A.offsets, A.E, A.rows, A.bpr, b0, b1);
     const uint64_t pol = l2_evict_first_policy();
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    unsigned long long n_blk = 0, n_scale = 0, n_elem = 0;
-    for (int64_t base = b0 + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; base < b1;
-         base += stride * kUnroll) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnroll;
+    Tally tally;
+    // warp-uniform loop: each warp takes kUnroll chunks of 32 consecutive blocks
+    for (int64_t base = b0 + warp * 32 * kUnroll; base < b1; base += step) {
         uint32_t w[kUnroll][16];
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + k * stride;
+            const int64_t blk = base + 32 * k + lane;
             if (blk < b1) {
                 const uint16_t* p = A.gu + blk * 32;
                 load_stream_32B(p, pol, w[k]);
                 load_stream_32B(p + 16, pol, w[k] + 8);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) w[k][j] = 0u;
             }
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + k * stride;
-            if (blk < b1) {
-                fused_block<kCount, kValues>(A, blk, w[k], n_scale, n_elem);
-                n_blk++;
-            }
+            const int64_t blk = base + 32 * k + lane;
+            fused_block<kCount, kValues, kBf16Clamp>(A, blk, blk < b1, w[k], tally);
         }
     }
     if (kCount) {
-        atomicAdd(A.counters + 0, n_blk);
-        if (n_scale) atomicAdd(A.counters + 1, n_scale);
-        if (n_elem) atomicAdd(A.counters + 2, n_elem);
+        atomicAdd(A.counters + 0, tally.blocks);
+        if (tally.scales) atomicAdd(A.counters + 1, tally.scales);
+        if (tally.nibbles) atomicAdd(A.counters + 2, tally.nibbles);
     }
 }
 
@@ -300,41 +398,40 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
 // Quantize-only
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kMinBlocksQuant)
 nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk,
                       uint8_t* __restrict__ packed, uint8_t* __restrict__ sf) {
     const uint64_t pol = l2_evict_first_policy();
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; base < nblk;
-         base += stride * kUnroll) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnroll;
+    for (int64_t base = warp * 32 * kUnroll; base < nblk; base += step) {
         uint32_t w[kUnroll][8];
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + k * stride;
+            const int64_t blk = base + 32 * k + lane;
             if (blk < nblk) load_stream_32B(x + blk * 16, pol, w[k]);
         }
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + k * stride;
+            const int64_t blk = base + 32 * k + lane;
             if (blk >= nblk) continue;
             float v[16];
-            float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                v[i] = (i & 1) ? bf16_hi(w[k][i >> 1]) : bf16_lo(w[k][i >> 1]);
-                amax = fmaxf(amax, fabsf(v[i]));
-            }
-            const uint32_t code = e4m3x2_rn_sat(0.0f, __fdiv_rn(amax, 6.0f)) & 0xFFu;
+            for (int i = 0; i < 16; i++) v[i] = (i & 1) ? bf16_hi(w[k][i >> 1]) : bf16_lo(w[k][i >> 1]);
+            const uint32_t code = e4m3x2_rn_sat(0.0f, div6(abs_max16(v))) & 0xFFu;
             const float d = e4m3_value(code);
-            const float inv = (code == 0u) ? 0.0f : __frcp_rn(d);
+            // any reciprocal within an ulp works: the corrected quotient
+            // below is exact at a tie, and elsewhere |x| / d sits at least
+            // 2^-13 (relative) away from every half-step boundary
+            const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
             float hs[16];
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 const float ax = fabsf(v[i]);
-                const float q0 = ax * inv;                       // |x| / d to ~1 ulp
-                const float r = fmaf(-q0, d, ax);                // exact residual
-                const float q1 = fmaf(r, inv, q0);               // correctly rounded |x| / d
-                hs[i] = with_sign_of(round_half_step(fminf(q1, 6.0f)), v[i]);
+                const float q0 = ax * inv;
+                const float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);     // |x| / d, corrected
+                hs[i] = with_sign_of((q1 + kHalfStepBias) - kHalfStepBias, v[i]);
             }
             *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(e2m1x8(hs), e2m1x8(hs + 8));
             sf[blk] = static_cast<uint8_t>(code);
@@ -349,10 +446,21 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk,
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    int occ_fused = 0, occ_fused_count = 0, occ_values = 0, occ_quant = 0;
+    int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};   // [bf16 clamp][plain, counted, values]
+    int occ_quant = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
+
+template <bool kBf16Clamp>
+bool fused_occupancy(int* occ) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[0], swiglu_nvfp4_kernel<false, false, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[1], swiglu_nvfp4_kernel<true, false, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[2], swiglu_nvfp4_kernel<false, true, kBf16Clamp>, kThreads, 0) == cudaSuccess;
+}
 
 int device_info(DeviceInfo& out) {
     int dev = 0;
@@ -362,12 +470,7 @@ int device_info(DeviceInfo& out) {
     if (!di.ready) {
         if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &di.occ_fused, swiglu_nvfp4_kernel<false, false>, kThreads, 0) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &di.occ_fused_count, swiglu_nvfp4_kernel<true, false>, kThreads, 0) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &di.occ_values, swiglu_nvfp4_kernel<false, true>, kThreads, 0) != cudaSuccess ||
+        if (!fused_occupancy<false>(di.occ[0]) || !fused_occupancy<true>(di.occ[1]) ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &di.occ_quant, nvfp4_quantize_kernel, kThreads, 0) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
@@ -377,9 +480,10 @@ int device_info(DeviceInfo& out) {
     return MOE_NVFP4_OK;
 }
 
+// Persistent grid: enough warps for the work, at most the resident CTAs.
 int grid_for(int64_t nblk, int sms, int occ) {
-    const int64_t want = (nblk + static_cast<int64_t>(kThreads) * kUnroll - 1) /
-                         (static_cast<int64_t>(kThreads) * kUnroll);
+    const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
+    const int64_t want = (nblk + per_cta - 1) / per_cta;
     const int64_t cap = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
 }
@@ -422,6 +526,30 @@ double window_for(float L) {
     return 2.0 * bound;
 }
 
+// BF16 bits of L when L is exactly a BF16 value, else -1.
+int64_t bf16_bits_of(float L) {
+    uint32_t b;
+    std::memcpy(&b, &L, 4);
+    if ((b & 0xFFFFu) != 0u) return -1;
+    return static_cast<int64_t>(b >> 16);
+}
+
+template <bool kBf16Clamp>
+void launch_fused_kernel(const FusedArgs& A, int64_t nblk, const DeviceInfo& di, bool counted,
+                         bool values, cudaStream_t stream) {
+    const int* occ = di.occ[kBf16Clamp ? 1 : 0];
+    if (values) {
+        swiglu_nvfp4_kernel<false, true, kBf16Clamp>
+            <<<grid_for(nblk, di.sms, occ[2]), kThreads, 0, stream>>>(A);
+    } else if (counted) {
+        swiglu_nvfp4_kernel<true, false, kBf16Clamp>
+            <<<grid_for(nblk, di.sms, occ[1]), kThreads, 0, stream>>>(A);
+    } else {
+        swiglu_nvfp4_kernel<false, false, kBf16Clamp>
+            <<<grid_for(nblk, di.sms, occ[0]), kThreads, 0, stream>>>(A);
+    }
+}
+
 int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_t* offsets,
                  int32_t E, uint8_t* packed, uint8_t* sf, uint64_t* counters, float* values,
                  cudaStream_t stream) {
@@ -436,18 +564,21 @@ int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     FusedArgs A;
-    A.gu = gu; A.rows = rows; A.bpr = I / 16; A.L = L; A.W = static_cast<float>(W);
+    A.gu = gu; A.rows = rows; A.bpr = I / 16; A.L = L;
+    const int64_t lb = bf16_bits_of(L);
+    const int64_t nlb = bf16_bits_of(-L);
+    A.L2 = lb < 0 ? 0u : static_cast<uint32_t>(lb) * 0x00010001u;
+    A.negL2 = nlb < 0 ? 0u : static_cast<uint32_t>(nlb) * 0x00010001u;
+    A.W = static_cast<float>(W);
+    A.Wp1 = static_cast<float>(1.0 + W);
+    A.Wm1 = static_cast<float>(1.0 - W);
+    A.near_thr = static_cast<float>(0.25 * (1.0 - W));
     A.offsets = (E > 0) ? offsets : nullptr; A.E = E;
     A.packed = packed; A.sf = sf;
     A.counters = reinterpret_cast<unsigned long long*>(counters); A.values = values;
     const int64_t nblk = rows * (I / 16);
-    if (values != nullptr) {
-        swiglu_nvfp4_kernel<false, true><<<grid_for(nblk, di.sms, di.occ_values), kThreads, 0, stream>>>(A);
-    } else if (counters != nullptr) {
-        swiglu_nvfp4_kernel<true, false><<<grid_for(nblk, di.sms, di.occ_fused_count), kThreads, 0, stream>>>(A);
-    } else {
-        swiglu_nvfp4_kernel<false, false><<<grid_for(nblk, di.sms, di.occ_fused), kThreads, 0, stream>>>(A);
-    }
+    if (lb >= 0) launch_fused_kernel<true>(A, nblk, di, counters != nullptr, values != nullptr, stream);
+    else launch_fused_kernel<false>(A, nblk, di, counters != nullptr, values != nullptr, stream);
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 

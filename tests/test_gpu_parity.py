@@ -229,6 +229,8 @@ def test_fast_path_error_is_inside_half_the_window():
             big = np.abs(y_ref) >= 2.0 ** -12
             rel = np.abs(y_fast[big].astype(np.float64) - y_ref[big]) / np.abs(y_ref[big])
             worst = max(worst, float(rel.max()))
+        print(f"\nL={L}: worst fast-path relative error {worst:.3e} "
+              f"(2^{np.log2(worst):.2f}), window {win:.3e}")
         assert worst <= win / 2, (L, worst, win)
 
 
