@@ -215,33 +215,44 @@ def device_buffers(w, torch, copies: int):
 
 
 def time_steps(torch, calls, steps: int, warmup: int, stream, flush=None):
-    """Warm up, then time exactly `steps` launches: total device time between
-    two events, plus each launch's own duration (event pairs on the launching
-    stream). `flush` (if given) runs between launches, outside the pairs."""
+    """Warm up, then time exactly `steps` launches back to back on the
+    launching stream: one event before, one after (barrier + synchronize on
+    both sides). Each step is one launch, so the mean launch duration is the
+    region's duration / steps. With `flush` (small inputs that fit in L2),
+    each launch is timed on its own event pair after an L2 flush instead."""
     for i in range(warmup):
         calls[i % len(calls)]()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    per = []
     wall0 = time.time()
-    t_begin.record(stream)
-    for i in range(steps):
-        if flush is not None:
+    if flush is None:
+        t_begin.record(stream)
+        for i in range(steps):
+            calls[i % len(calls)]()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    else:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        t_begin.record(stream)
+        for i in range(steps):
             flush()
-        starts[i].record(stream)
-        calls[i % len(calls)]()
-        ends[i].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+            starts[i].record(stream)
+            calls[i % len(calls)]()
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        per = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
     barrier()
     torch.cuda.synchronize()
     wall1 = time.time()
     total_s = t_begin.elapsed_time(t_end) / 1e3
-    per = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    if not per:
+        per = [total_s / steps] * steps
     return total_s, per, wall0, wall1
 
 
@@ -345,7 +356,7 @@ def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str
             "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
             "peak_source": f"{peak_src} (hbm_gbs, burst copy)",
             "launch_us_mean": round(mean_s * 1e6, 2),
-            "launch_us_median": round(statistics.median(per_launch_s) * 1e6, 2)}
+            "timing": "mean launch = timed region / launches (back-to-back on one stream)"}
 
 
 def main_ours(args):

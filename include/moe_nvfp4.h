@@ -29,8 +29,9 @@
  * rounded once to fp32. The fused kernel computes y_i with fast fp32
  * arithmetic (relative error far below the window below) and, wherever a
  * fast value lies within the window of a rounding boundary of the scale or
- * of a nibble, re-evaluates it in double precision, so its scale and nibble
- * decisions are those of the definition. Quantize-only is exact throughout.
+ * of a nibble, re-evaluates it with about 46 significant bits (double-float
+ * arithmetic), so its scale and nibble decisions are those of the
+ * definition. Quantize-only is exact throughout.
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, row-major,
@@ -121,6 +122,15 @@ MOE_NVFP4_API int moe_swiglu_fast_values(const uint16_t *gu, int64_t rows, int64
                            float *y, moe_nvfp4_stream_t stream);
 
 /*
+ * Diagnostic: the fp32 SwiGLU values y [rows, I] by the definition (the
+ * formula evaluated with about 46 significant bits and rounded once to fp32),
+ * as the fused kernel computes them wherever a fast value falls inside its
+ * decision window. Same argument rules as moe_swiglu_fast_values.
+ */
+MOE_NVFP4_API int moe_swiglu_precise_values(const uint16_t *gu, int64_t rows, int64_t I,
+                                            float clamp_L, float *y, moe_nvfp4_stream_t stream);
+
+/*
  * Diagnostic: as moe_swiglu_nvfp4_quantize, and also adds to the caller's
  * DEVICE counters (uint64 [3], not cleared by the call):
  *   [0] blocks processed, [1] blocks whose scale needed the re-evaluation,
@@ -133,7 +143,7 @@ MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_counted(const uint16_t *gu, int64_t 
 
 /* The relative window the fused kernel uses for a clamp L: a scale or
  * nibble decision whose fast-path input lies within this relative distance
- * of a rounding boundary is redone from a double-precision SwiGLU value.
+ * of a rounding boundary is redone from the definition's SwiGLU value.
  * It bounds the fast path's relative error (fp32 exponent-argument rounding,
  * which grows with the most negative gate that can still reach a nonzero
  * nibble for this L, plus the approximate exp2 and reciprocal), with a

@@ -17,6 +17,7 @@ import os
 from . import build as _build
 
 __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_values",
+           "moe_swiglu_precise_values",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
 
@@ -50,6 +51,8 @@ def load_library():
     lib.moe_swiglu_nvfp4_quantize.restype = ctypes.c_int
     lib.moe_swiglu_fast_values.argtypes = [P, I64, I64, F, P, P]
     lib.moe_swiglu_fast_values.restype = ctypes.c_int
+    lib.moe_swiglu_precise_values.argtypes = [P, I64, I64, F, P, P]
+    lib.moe_swiglu_precise_values.restype = ctypes.c_int
     lib.moe_swiglu_nvfp4_quantize_counted.argtypes = [P, I64, I64, F, P, I32, P, P, P, P]
     lib.moe_swiglu_nvfp4_quantize_counted.restype = ctypes.c_int
     lib.moe_swiglu_nvfp4_window.argtypes = [F]
@@ -193,4 +196,19 @@ def moe_swiglu_fast_values(gu, clamp_L: float, stream=None):
             ctypes.c_void_p(gu.data_ptr()), rows, two_i // 2, float(clamp_L),
             ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream))
     _check(rc, "moe_swiglu_fast_values")
+    return y
+
+
+def moe_swiglu_precise_values(gu, clamp_L: float, stream=None):
+    """Diagnostic: the definition-path fp32 SwiGLU values [rows, I] (what the
+    fused kernel uses inside its decision window)."""
+    torch = _torch()
+    gu = _bf16_bits(gu, "gu", 32)
+    rows, two_i = gu.shape
+    y = torch.empty((rows, two_i // 2), dtype=torch.float32, device=gu.device)
+    with torch.cuda.device(gu.device):
+        rc = load_library().moe_swiglu_precise_values(
+            ctypes.c_void_p(gu.data_ptr()), rows, two_i // 2, float(clamp_L),
+            ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_swiglu_precise_values")
     return y

@@ -18,9 +18,10 @@
 //     row r reads the 64 contiguous input bytes gu[r, 32b .. 32b+31] (or the
 //     32 bytes x[r, 16b .. 16b+15]) and writes 8 packed bytes + 1 scale
 //     byte, all at index r * (I/16) + b. Row boundaries never split a block,
-//     so a thread walks blocks in a grid-stride loop over [first, last) of
-//     the active rows, with 256-bit L1-bypassing loads marked evict-first in
-//     L2 (the stream is read once) and U blocks in flight per thread.
+//     so the active blocks [first, last) are split into equal contiguous
+//     ranges, one per resident CTA, whose warps claim 64-block chunks from a
+//     shared counter; loads are 256-bit, L1-bypassing and marked evict-first
+//     in L2 (the stream is read once), two blocks in flight per lane.
 //   * Each thread owns whole blocks, so the amax needs no shuffles.
 //   * E4M3 scale: cvt.rn.satfinite.e4m3x2.f32 (RNE, saturating at 448);
 //     E2M1 nibbles: the half step is rounded with the exact fp32 trick
@@ -30,7 +31,8 @@
 //   * Fused path: SwiGLU in fast fp32 (ex2.approx + rcp.approx). A scale or
 //     nibble decision whose input lies within a relative window W of a
 //     rounding boundary (W bounds the fast path's error, with margin) is
-//     redone from a double-precision SwiGLU value, the definition's value.
+//     redone from the definition's value, evaluated in double-float
+//     arithmetic (~46 bits) on the FP32 pipes.
 //     Quantize-only: exact division by a Markstein correction
 //     (q = x*rcp_rn(d), r = fma(-q, d, x), q' = fma(r, rcp_rn(d), q)).
 #include <cuda_fp16.h>
@@ -46,7 +48,8 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;                 // blocks in flight per lane
+constexpr int kUnroll = 2;                 // blocks in flight per lane (fused)
+constexpr int kUnrollQuant = 4;            // blocks in flight per lane (quantize-only)
 constexpr int kMinBlocksFused = 3;         // resident CTAs per SM the register budget targets
 constexpr int kMinBlocksQuant = 4;
 constexpr int kMaxDevices = 64;
@@ -177,6 +180,143 @@ __device__ __noinline__ float swiglu_double(float g, float u, float L) {
     return __double2float_rn(y);
 }
 
+// ---------------------------------------------------------------------------
+// The definition's value in double-float arithmetic
+// ---------------------------------------------------------------------------
+// A value is carried as the unevaluated sum hi + lo of two fp32 numbers
+// (|lo| <= ulp(hi) / 2), about 46 significant bits: rounding the result to
+// fp32 then agrees with a double-precision evaluation unless the exact value
+// lies within ~2^-44 (relative) of an fp32 rounding midpoint. It runs on the
+// FP32 pipes with a short dependency chain; GB300's FP64 pipe is narrow and
+// slow, and one double-precision evaluation on a warp's critical path
+// lengthens the whole launch by its latency (the last such element ends the
+// kernel late). The explicit _rn intrinsics keep the compiler from fusing
+// the error-free transformations into FMAs.
+
+struct DFloat {
+    float hi, lo;
+};
+
+__device__ __forceinline__ DFloat df_two_sum(float a, float b) {          // exact a + b
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ DFloat df_fast_two_sum(float a, float b) {     // |a| >= |b|
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ DFloat df_two_prod(float a, float b) {         // exact a * b
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ DFloat df_add(DFloat a, DFloat b) {
+    const DFloat s = df_two_sum(a.hi, b.hi);
+    return df_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ DFloat df_mul(DFloat a, DFloat b) {
+    const float p = __fmul_rn(a.hi, b.hi);
+    float e = __fmaf_rn(a.hi, b.hi, -p);
+    e = __fmaf_rn(a.hi, b.lo, e);
+    e = __fmaf_rn(a.lo, b.hi, e);
+    return df_fast_two_sum(p, e);
+}
+
+// ln 2 / 64 = kLn2x64Hi + kLn2x64Mid + kLn2x64Lo; the head has 9 significant
+// bits, so n * head is exact for |n| < 2^15.
+constexpr float kInvLn2x64 = 0x1.715476p+6f;       // 64 / ln 2
+constexpr float kLn2x64Hi = 0x1.63p-7f;
+constexpr float kLn2x64Mid = -0x1.bd0106p-19f;
+constexpr float kLn2x64Lo = 0x1.cf79acp-46f;
+
+// 2^(j/64) = hi + lo for j = 0..63.
+__constant__ float2 kExp2Table[64] = {
+    {0x1.0p+0f, 0.0f}, {0x1.02c9a4p+0f, -0x1.887fap-28f},
+    {0x1.059b0ep+0f, -0x1.9d4f52p-25f}, {0x1.087452p+0f, -0x1.e2990ep-26f},
+    {0x1.0b5586p+0f, 0x1.9f3122p-25f}, {0x1.0e3ec4p+0f, -0x1.a585ccp-25f},
+    {0x1.11301ep+0f, -0x1.fdb496p-25f}, {0x1.1429aap+0f, 0x1.d525bcp-25f},
+    {0x1.172b84p+0f, -0x1.c15742p-27f}, {0x1.1a35bep+0f, 0x1.6df96ep-25f},
+    {0x1.1d4874p+0f, -0x1.d2e8cap-25f}, {0x1.2063b8p+0f, 0x1.0c519ap-25f},
+    {0x1.2387a6p+0f, 0x1.ceac48p-25f}, {0x1.26b456p+0f, 0x1.789f38p-26f},
+    {0x1.29e9ep+0f, -0x1.5c0424p-25f}, {0x1.2d285ap+0f, 0x1.b900c2p-26f},
+    {0x1.306fep+0f, 0x1.4636e2p-25f}, {0x1.33c08cp+0f, -0x1.b37d2p-25f},
+    {0x1.371a74p+0f, -0x1.18aac6p-25f}, {0x1.3a7db4p+0f, -0x1.634c02p-25f},
+    {0x1.3dea64p+0f, 0x1.824684p-25f}, {0x1.4160a2p+0f, 0x1.f72e2ap-28f},
+    {0x1.44e086p+0f, 0x1.8624b4p-30f}, {0x1.486a2cp+0f, -0x1.47d866p-25f},
+    {0x1.4bfdaep+0f, -0x1.593abcp-25f}, {0x1.4f9b28p+0f, -0x1.2c5a6cp-25f},
+    {0x1.5342b6p+0f, -0x1.2c561p-25f}, {0x1.56f474p+0f, -0x1.295b04p-25f},
+    {0x1.5ab07ep+0f, -0x1.5bd5ecp-27f}, {0x1.5e76f2p+0f, -0x1.4a5bd6p-25f},
+    {0x1.6247ecp+0f, -0x1.f8b55p-25f}, {0x1.662388p+0f, 0x1.2a9112p-27f},
+    {0x1.6a09e6p+0f, 0x1.9fcef4p-26f}, {0x1.6dfb24p+0f, -0x1.cd72e8p-27f},
+    {0x1.71f75ep+0f, 0x1.1d8beep-25f}, {0x1.75feb6p+0f, -0x1.37b306p-25f},
+    {0x1.7a1148p+0f, -0x1.829fdp-25f}, {0x1.7e2f34p+0f, -0x1.261634p-25f},
+    {0x1.82589ap+0f, -0x1.accc7cp-26f}, {0x1.868d9ap+0f, -0x1.2edb44p-26f},
+    {0x1.8ace54p+0f, 0x1.15506ep-27f}, {0x1.8f1aeap+0f, -0x1.baa232p-26f},
+    {0x1.93737cp+0f, -0x1.e64744p-25f}, {0x1.97d82ap+0f, -0x1.0d8d84p-31f},
+    {0x1.9c4918p+0f, 0x1.51f848p-27f}, {0x1.a0c668p+0f, -0x1.2886a6p-26f},
+    {0x1.a5503cp+0f, -0x1.b83b54p-25f}, {0x1.a9e6b6p+0f, -0x1.50c048p-25f},
+    {0x1.ae89fap+0f, -0x1.a94b14p-26f}, {0x1.b33a2cp+0f, -0x1.ec3a82p-26f},
+    {0x1.b7f77p+0f, -0x1.a09438p-25f}, {0x1.bcc1eap+0f, -0x1.f687c6p-25f},
+    {0x1.c199bep+0f, -0x1.3d56b2p-27f}, {0x1.c67f12p+0f, 0x1.cafa2ap-25f},
+    {0x1.cb720ep+0f, -0x1.8837ccp-27f}, {0x1.d072d4p+0f, 0x1.40f13p-25f},
+    {0x1.d5818ep+0f, -0x1.822dbcp-27f}, {0x1.da9e6p+0f, 0x1.ed9942p-27f},
+    {0x1.dfc974p+0f, -0x1.908c94p-25f}, {0x1.e502eep+0f, 0x1.e2cffep-26f},
+    {0x1.ea4afap+0f, 0x1.52486cp-27f}, {0x1.efa1bep+0f, 0x1.cc2b44p-25f},
+    {0x1.f50766p+0f, -0x1.246ebp-26f}, {0x1.fa7c18p+0f, 0x1.9e90d8p-28f},
+};
+
+// e^x for -100 <= x <= 80 as a double-float: x = n ln2/64 + r with
+// |r| <= ln2/128, e^x = 2^(n/64) e^r, e^r by its Taylor series to r^5 (the
+// r^3.. terms in fp32, the rest in double-float).
+__device__ __forceinline__ DFloat exp_df(float x) {
+    const float nf = rintf(__fmul_rn(x, kInvLn2x64));
+    const int n = __float2int_rn(nf);
+    const float r1 = __fmaf_rn(-nf, kLn2x64Hi, x);          // exact
+    const DFloat t = df_two_prod(nf, kLn2x64Mid);
+    DFloat r = df_two_sum(r1, -t.hi);
+    r = df_fast_two_sum(r.hi, __fadd_rn(r.lo, __fmaf_rn(-nf, kLn2x64Lo, -t.lo)));
+    const float rh = r.hi;
+    const float tail = __fmul_rn(__fmul_rn(rh, __fmul_rn(rh, rh)),
+                                 __fmaf_rn(rh, __fmaf_rn(rh, 1.0f / 120.0f, 1.0f / 24.0f), 1.0f / 6.0f));
+    DFloat sq = df_two_prod(rh, rh);
+    sq.lo = __fmaf_rn(__fmul_rn(2.0f, rh), r.lo, sq.lo);
+    const DFloat half_sq = {__fmul_rn(sq.hi, 0.5f), __fmul_rn(sq.lo, 0.5f)};
+    DFloat s = df_add(half_sq, DFloat{tail, 0.0f});
+    s = df_add(r, s);
+    s = df_add(DFloat{1.0f, 0.0f}, s);
+    const float2 tj = kExp2Table[n & 63];
+    DFloat e = df_mul(DFloat{tj.x, tj.y}, s);
+    const int k = n >> 6;                                      // floor(n / 64)
+    e.hi = ldexpf(e.hi, k);
+    e.lo = ldexpf(e.lo, k);
+    return e;
+}
+
+// The definition's value: silu(min(g, L)) * clamp(u, -L, L) rounded once to
+// fp32, from a double-float evaluation (a gate below -80 falls back to
+// double precision; such an element is far too small to reach any rounding
+// decision, so the fallback only keeps the function total).
+__device__ __noinline__ float swiglu_precise(float g, float u, float L) {
+    const float a = fminf(g, L);
+    const float b = fminf(fmaxf(u, -L), L);
+    if (a < -80.0f) return swiglu_double(g, u, L);
+    DFloat sig = {1.0f, 0.0f};                                 // e^-a underflows
+    if (a <= 100.0f) {
+        const DFloat den = df_add(DFloat{1.0f, 0.0f}, exp_df(-a));
+        const float y0 = __frcp_rn(den.hi);
+        float eps = __fmaf_rn(-den.hi, y0, 1.0f);              // exact residual
+        eps = __fmaf_rn(-den.lo, y0, eps);
+        sig = df_fast_two_sum(y0, __fmul_rn(y0, eps));         // 1 / (1 + e^-a)
+    }
+    const DFloat ab = df_two_prod(a, b);
+    const DFloat y = df_mul(ab, sig);
+    return copysignf(y.hi, ab.hi);
+}
+
 // gate / up of output i (0..15) of the block starting at `blk_in`.
 __device__ __forceinline__ void gate_up_at(const uint16_t* blk_in, int i, float& g, float& u) {
     const int grp = i >> 3, j = i & 7;
@@ -238,8 +378,8 @@ __device__ __forceinline__ void active_block_range(const int32_t* offsets, int E
 
 // Scale code of a block whose fast amax lies within the window of an E4M3
 // rounding boundary: every element that could be the true maximum is
-// re-evaluated in double precision (and replaced in y), then the code is
-// taken from the exact amax.
+// re-evaluated by the definition (and replaced in y), then the code is taken
+// from the exact amax.
 __device__ __forceinline__ uint32_t scale_by_definition(const uint16_t* blk_in, float L, float W,
                                                         float amax, float* y) {
     const float lim = amax * (1.0f - 2.0f * W);
@@ -249,7 +389,7 @@ __device__ __forceinline__ uint32_t scale_by_definition(const uint16_t* blk_in, 
         if (fabsf(y[i]) >= lim) {
             float g, u;
             gate_up_at(blk_in, i, g, u);
-            y[i] = swiglu_double(g, u, L);
+            y[i] = swiglu_precise(g, u, L);
         }
         am = fmaxf(am, fabsf(y[i]));
     }
@@ -334,14 +474,14 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
                 }
             }
         }
-        // one double-precision SwiGLU per lane per pass, all lanes together
+        // one definition-path SwiGLU per lane per pass, all lanes together
         while (__any_sync(kFullMask, todo != 0u)) {
             if (todo != 0u) {
                 const int i = __ffs(todo) - 1;
                 todo &= todo - 1u;
                 float g, u;
                 gate_up_at(blk_in, i, g, u);
-                const uint32_t nib = nibble_by_definition(swiglu_double(g, u, L), d, code);
+                const uint32_t nib = nibble_by_definition(swiglu_precise(g, u, L), d, code);
                 const int sh = 4 * (i & 7);
                 if (i < 8) lo = (lo & ~(0xFu << sh)) | (nib << sh);
                 else       hi = (hi & ~(0xFu << sh)) | (nib << sh);
@@ -363,16 +503,31 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
     active_block_range(A.offsets, A.E, A.rows, A.bpr, b0, b1);
     const uint64_t pol = l2_evict_first_policy();
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnroll;
+    // Each CTA owns an equal contiguous range of blocks; its warps claim
+    // chunks of 32 * kUnroll blocks from a shared counter, so a warp held up
+    // by a rare exact re-evaluation (or slow memory) takes fewer chunks and
+    // the CTA's other warps absorb the delay.
+    constexpr int64_t kChunk = 32 * kUnroll;
+    const int64_t total = b1 - b0;
+    int64_t per_cta = (total + gridDim.x - 1) / gridDim.x;
+    per_cta = (per_cta + kChunk - 1) / kChunk * kChunk;
+    const int64_t cta_begin = b0 + static_cast<int64_t>(blockIdx.x) * per_cta;
+    const int64_t cta_end = cta_begin + per_cta < b1 ? cta_begin + per_cta : b1;
+    __shared__ int next_chunk;
+    if (threadIdx.x == 0) next_chunk = 0;
+    __syncthreads();
     Tally tally;
-    // warp-uniform loop: each warp takes kUnroll chunks of 32 consecutive blocks
-    for (int64_t base = b0 + warp * 32 * kUnroll; base < b1; base += step) {
+    for (;;) {                                              // warp-uniform
+        int c = 0;
+        if (lane == 0) c = atomicAdd(&next_chunk, 1);
+        c = __shfl_sync(kFullMask, c, 0);
+        const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
+        if (base >= cta_end) break;
         uint32_t w[kUnroll][16];
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
             const int64_t blk = base + 32 * k + lane;
-            if (blk < b1) {
+            if (blk < cta_end) {
                 const uint16_t* p = A.gu + blk * 32;
                 load_stream_32B(p, pol, w[k]);
                 load_stream_32B(p + 16, pol, w[k] + 8);
@@ -384,13 +539,28 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
             const int64_t blk = base + 32 * k + lane;
-            fused_block<kCount, kValues, kBf16Clamp>(A, blk, blk < b1, w[k], tally);
+            fused_block<kCount, kValues, kBf16Clamp>(A, blk, blk < cta_end, w[k], tally);
         }
     }
     if (kCount) {
         atomicAdd(A.counters + 0, tally.blocks);
         if (tally.scales) atomicAdd(A.counters + 1, tally.scales);
         if (tally.nibbles) atomicAdd(A.counters + 2, tally.nibbles);
+    }
+}
+
+// Diagnostic: the definition-path SwiGLU value of every output element.
+__global__ void swiglu_precise_values_kernel(const uint16_t* __restrict__ gu, int64_t rows,
+                                             int64_t I, float L, float* __restrict__ y) {
+    const int64_t n = rows * I;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = idx / I, c = idx % I;
+        const uint16_t* row = gu + r * 2 * I;
+        const int64_t gc = 16 * (c / 8) + (c % 8);
+        const float g = __uint_as_float(static_cast<uint32_t>(row[gc]) << 16);
+        const float u = __uint_as_float(static_cast<uint32_t>(row[gc + 8]) << 16);
+        y[idx] = swiglu_precise(g, u, L);
     }
 }
 
@@ -404,16 +574,16 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk,
     const uint64_t pol = l2_evict_first_policy();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnroll;
-    for (int64_t base = warp * 32 * kUnroll; base < nblk; base += step) {
-        uint32_t w[kUnroll][8];
+    const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnrollQuant;
+    for (int64_t base = warp * 32 * kUnrollQuant; base < nblk; base += step) {
+        uint32_t w[kUnrollQuant][8];
 #pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
+        for (int k = 0; k < kUnrollQuant; k++) {
             const int64_t blk = base + 32 * k + lane;
             if (blk < nblk) load_stream_32B(x + blk * 16, pol, w[k]);
         }
 #pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
+        for (int k = 0; k < kUnrollQuant; k++) {
             const int64_t blk = base + 32 * k + lane;
             if (blk >= nblk) continue;
             float v[16];
@@ -481,8 +651,8 @@ int device_info(DeviceInfo& out) {
 }
 
 // Persistent grid: enough warps for the work, at most the resident CTAs.
-int grid_for(int64_t nblk, int sms, int occ) {
-    const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
+int grid_for(int64_t nblk, int sms, int occ, int unroll = kUnroll) {
+    const int64_t per_cta = static_cast<int64_t>(kThreads) * unroll;
     const int64_t want = (nblk + per_cta - 1) / per_cta;
     const int64_t cap = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
@@ -593,7 +763,7 @@ int moe_nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* pack
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     const int64_t nblk = rows * (K / 16);
-    nvfp4_quantize_kernel<<<grid_for(nblk, di.sms, di.occ_quant), kThreads, 0,
+    nvfp4_quantize_kernel<<<grid_for(nblk, di.sms, di.occ_quant, kUnrollQuant), kThreads, 0,
                             reinterpret_cast<cudaStream_t>(stream)>>>(x, nblk, packed, sf);
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
@@ -610,6 +780,19 @@ int moe_swiglu_fast_values(const uint16_t* gu, int64_t rows, int64_t I, float cl
     if (rows > 0 && y == nullptr) return MOE_NVFP4_ENULL;
     return launch_fused(gu, rows, I, clamp_L, nullptr, 0, nullptr, nullptr, nullptr, y,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_swiglu_precise_values(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
+                               float* y, moe_nvfp4_stream_t stream) {
+    int rc = check_common(gu, rows, I, 4, y, y);
+    if (rc != MOE_NVFP4_OK) return rc;
+    if (window_for(clamp_L) < 0.0) return MOE_NVFP4_ECLAMP;
+    if (rows == 0) return MOE_NVFP4_OK;
+    DeviceInfo di;
+    if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    swiglu_precise_values_kernel<<<di.sms * 8, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        gu, rows, I, clamp_L, y);
+    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 
 int moe_swiglu_nvfp4_quantize_counted(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,

@@ -234,6 +234,44 @@ def test_fast_path_error_is_inside_half_the_window():
         assert worst <= win / 2, (L, worst, win)
 
 
+def test_precise_path_matches_the_oracle_on_every_bf16_gate():
+    """The values the fused kernel falls back to inside its window (a
+    double-float evaluation) equal the oracle's double-precision ones, bit
+    for bit, except where the exact value lies so close to an fp32 rounding
+    midpoint that neither evaluation can decide it (checked with 60-digit
+    decimals)."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 60
+    gates = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    gates = gates[np.isfinite(W.bf16_to_f32(gates))]
+    rng = np.random.default_rng(31)
+    for L in (7.0, 10.0):
+        for uval in (1.0, L, -L / 3, None):
+            if uval is None:
+                up = W.bf16_bits((rng.standard_normal(gates.size) * 3).astype(np.float32))
+            else:
+                up = W.bf16_bits(np.full(gates.shape, uval, np.float32))
+            n = gates.size - gates.size % 16
+            gu = W.interleave_gate_up(gates[:n].reshape(-1, 16), up[:n].reshape(-1, 16))
+            y_gpu = M.moe_swiglu_precise_values(dev(gu), L).cpu().numpy().ravel()
+            y_ref = oracle.swiglu_values(gu, L).ravel()
+            bad = np.nonzero(y_gpu.view(np.uint32) != y_ref.view(np.uint32))[0]
+            g_all = W.bf16_to_f32(gates[:n]); u_all = W.bf16_to_f32(up[:n])
+            for k in bad:
+                a = min(float(g_all[k]), L)
+                b = min(max(float(u_all[k]), -L), L)
+                A, B = Decimal(a), Decimal(b)
+                exact = A / (1 + (-A).exp()) * B
+                lo_v, hi_v = sorted([float(y_gpu[k]), float(y_ref[k])])
+                mid = (Decimal(lo_v) + Decimal(hi_v)) / 2
+                assert abs(exact - mid) <= abs(exact) * Decimal(2) ** -40, (a, b, y_gpu[k], y_ref[k])
+            # undecidable points come from tiny gates (y = L a/2 + L a^2/4 - ...
+            # with the first two terms on a midpoint); none can reach a rounding
+            # decision, which needs |y| >= 2^-12 (a quarter of the smallest
+            # nonzero scale, with margin)
+            assert not np.any(np.abs(y_ref[bad]) >= 2.0 ** -12), (L, uval, y_ref[bad])
+
+
 def test_side_stream_and_graph_replay_with_new_offsets():
     w = W.ragged_routing(tokens=256, experts=8, topk=4, I=512, pad_rows=11)
     gu = dev(w.data)
