@@ -144,10 +144,12 @@ MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_counted(const uint16_t *gu, int64_t 
 /* The relative window the fused kernel uses for a clamp L: a scale or
  * nibble decision whose fast-path input lies within this relative distance
  * of a rounding boundary is redone from the definition's SwiGLU value.
- * It bounds the fast path's relative error (fp32 exponent-argument rounding,
- * which grows with the most negative gate that can still reach a nonzero
- * nibble for this L, plus the approximate exp2 and reciprocal), with a
- * factor 2 of margin. Returns a negative value for an invalid L. */
+ * It bounds the fast path's relative error with margin: when every gate
+ * that can still reach a nonzero nibble for this L is >= -16 (L up to about
+ * 135), from the fast silu's largest error over every BF16 gate >= -16
+ * (measured exhaustively by the test suite) plus four roundings, times 1.5;
+ * beyond that, from an analytic bound that grows with the most negative
+ * such gate, times 2. Returns a negative value for an invalid L. */
 MOE_NVFP4_API double moe_swiglu_nvfp4_window(float clamp_L);
 
 /* Static text for a return code. */

@@ -209,29 +209,47 @@ def test_zero_rows_is_a_no_op():
     assert p.shape == (0, 16) and s.shape == (0, 2) and q.shape == (0, 16) and t.shape == (0, 2)
 
 
-def test_fast_path_error_is_inside_half_the_window():
-    """The window doubles an analytic error bound of the fast path; the
-    measured error over every BF16 gate (with up = 1 and up = L) must stay
-    inside that bound."""
-    gates = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
-    gf = W.bf16_to_f32(gates)
-    finite = np.isfinite(gf)
-    gates, gf = gates[finite], gf[finite]
+def _fast_vs_oracle(gates, uval, L):
+    up = W.bf16_bits(np.full(gates.shape, uval, np.float32))
+    n = gates.size - gates.size % 16
+    gu = W.interleave_gate_up(gates[:n].reshape(-1, 16), up[:n].reshape(-1, 16))
+    y_fast = M.moe_swiglu_fast_values(dev(gu), L).cpu().numpy().ravel().astype(np.float64)
+    y_ref = oracle.swiglu_values(gu, L).ravel().astype(np.float64)
+    return y_fast, y_ref
+
+
+def test_fast_path_error_is_inside_the_window():
+    """For L up to ~135 the kernel's window rests on one measured constant:
+    the fast silu's largest relative error over every BF16 gate >= -16 (the
+    only gates that can reach a rounding decision there). Measure it
+    exhaustively (up = 1, so the product is exact) and check the constant
+    the window implies; then check whole SwiGLU values for L = 7 and 10, and
+    the analytic regime for a large L."""
+    allg = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    gv = W.bf16_to_f32(allg)
+    gates = allg[np.isfinite(gv) & (gv >= -16.0)]
+    u24 = 2.0 ** -24
+    y_fast, y_ref = _fast_vs_oracle(gates, 1.0, 100.0)
+    nz = y_ref != 0
+    e_silu = float(np.max(np.abs(y_fast[nz] - y_ref[nz]) / np.abs(y_ref[nz])))
+    e_const = M.moe_swiglu_nvfp4_window(100.0) / 1.5 - 5 * u24
+    print(f"\nfast silu: worst relative error {e_silu:.3e} (2^{np.log2(e_silu):.2f}) "
+          f"over {gates.size} gates >= -16; bound used {e_const:.3e}")
+    assert e_silu <= e_const
     for L in (7.0, 10.0):
         win = M.moe_swiglu_nvfp4_window(L)
-        worst = 0.0
-        for uval in (1.0, L, -L / 3):
-            up = W.bf16_bits(np.full(gates.shape, uval, np.float32))
-            n = gates.size - gates.size % 16
-            gu = W.interleave_gate_up(gates[:n].reshape(-1, 16), up[:n].reshape(-1, 16))
-            y_fast = M.moe_swiglu_fast_values(dev(gu), L).cpu().numpy().ravel()
-            y_ref = oracle.swiglu_values(gu, L).ravel()
+        for uval in (L, -L / 3, 1.7):
+            y_fast, y_ref = _fast_vs_oracle(gates, uval, L)
             big = np.abs(y_ref) >= 2.0 ** -12
-            rel = np.abs(y_fast[big].astype(np.float64) - y_ref[big]) / np.abs(y_ref[big])
-            worst = max(worst, float(rel.max()))
-        print(f"\nL={L}: worst fast-path relative error {worst:.3e} "
-              f"(2^{np.log2(worst):.2f}), window {win:.3e}")
-        assert worst <= win / 2, (L, worst, win)
+            rel = np.abs(y_fast[big] - y_ref[big]) / np.abs(y_ref[big])
+            # y's error budget inside the window: silu, product, definition rounding
+            assert rel.max() <= win / 1.5 - 2 * u24, (L, uval, rel.max(), win)
+    L = 4000.0                                     # analytic regime: gates down to ~ -22
+    allf = allg[np.isfinite(gv)]
+    y_fast, y_ref = _fast_vs_oracle(allf, 1.0, L)
+    big = np.abs(y_ref) * L >= 2.0 ** -12
+    rel = np.abs(y_fast[big] - y_ref[big]) / np.abs(y_ref[big])
+    assert rel.max() <= M.moe_swiglu_nvfp4_window(L) / 2, (rel.max(), M.moe_swiglu_nvfp4_window(L))
 
 
 def test_precise_path_matches_the_oracle_on_every_bf16_gate():
