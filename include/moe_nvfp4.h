@@ -46,6 +46,15 @@
  *    nothing and leaves the outputs untouched. Faults inside a launched
  *    kernel surface, as with any CUDA launch, at the caller's next
  *    synchronisation.
+ *  - Kernels are launched with programmatic stream serialization
+ *    (programmatic dependent launch): each one waits until the preceding
+ *    work in the stream has completed and is visible before it reads any
+ *    memory, so stream order holds as usual, while its launch overlaps the
+ *    tail of the preceding kernel. It also lets the kernel after it launch
+ *    early; a following kernel that is itself launched with that attribute
+ *    must wait for its dependency (griddepcontrol.wait /
+ *    cudaGridDependencySynchronize) before reading these outputs, as any
+ *    programmatic-launch consumer must.
  *  - The library caches, per device, the SM count and the kernels'
  *    occupancy on first use; it is otherwise stateless and thread-safe.
  */

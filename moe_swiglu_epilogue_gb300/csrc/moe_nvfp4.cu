@@ -42,6 +42,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "moe_nvfp4.h"
 
@@ -74,6 +75,16 @@ __device__ __forceinline__ void load_stream_32B(const void* p, uint64_t pol, uin
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
           "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
         : "l"(p), "l"(pol));
+}
+
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (a no-op without a programmatic
+// dependency), then let the next grid start launching.
+__device__ __forceinline__ void wait_for_preceding_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_next_grid_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -433,9 +444,10 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
     }
     const uint16_t* blk_in = A.gu + blk * 32;
 
-    // scale: safe when both ends of the window round to the same code
+    // scale: safe when both ends of the window round to the same code (the
+    // product by RN(1/6) is within an ulp of amax / 6, inside the window)
     const float amax = abs_max16(y);
-    const float q = div6(amax);
+    const float q = amax * kInv6;
     const uint32_t ends = e4m3x2_rn_sat(q * A.Wp1, q * A.Wm1);
     uint32_t code = ends & 0xFFu;
     if (valid && (ends >> 8) != code) {
@@ -499,6 +511,8 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
 template <bool kCount, bool kValues, bool kBf16Clamp>
 __global__ void __launch_bounds__(kThreads, kMinBlocksFused)
 swiglu_nvfp4_kernel(const FusedArgs A) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
     int64_t b0, b1;
     active_block_range(A.offsets, A.E, A.rows, A.bpr, b0, b1);
     const uint64_t pol = l2_evict_first_policy();
@@ -552,6 +566,8 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
 // Diagnostic: the definition-path SwiGLU value of every output element.
 __global__ void swiglu_precise_values_kernel(const uint16_t* __restrict__ gu, int64_t rows,
                                              int64_t I, float L, float* __restrict__ y) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
     const int64_t n = rows * I;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -571,6 +587,8 @@ __global__ void swiglu_precise_values_kernel(const uint16_t* __restrict__ gu, in
 __global__ void __launch_bounds__(kThreads, kMinBlocksQuant)
 nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk,
                       uint8_t* __restrict__ packed, uint8_t* __restrict__ sf) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
     const uint64_t pol = l2_evict_first_policy();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
@@ -717,19 +735,34 @@ int64_t bf16_bits_of(float L) {
     return static_cast<int64_t>(b >> 16);
 }
 
+// Launch with programmatic stream serialization, so this grid's launch
+// overlaps the tail of the preceding one (each kernel above waits for it
+// before touching memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <bool kBf16Clamp>
 void launch_fused_kernel(const FusedArgs& A, int64_t nblk, const DeviceInfo& di, bool counted,
                          bool values, cudaStream_t stream) {
     const int* occ = di.occ[kBf16Clamp ? 1 : 0];
     if (values) {
-        swiglu_nvfp4_kernel<false, true, kBf16Clamp>
-            <<<grid_for(nblk, di.sms, occ[2]), kThreads, 0, stream>>>(A);
+        launch(swiglu_nvfp4_kernel<false, true, kBf16Clamp>, grid_for(nblk, di.sms, occ[2]), stream, A);
     } else if (counted) {
-        swiglu_nvfp4_kernel<true, false, kBf16Clamp>
-            <<<grid_for(nblk, di.sms, occ[1]), kThreads, 0, stream>>>(A);
+        launch(swiglu_nvfp4_kernel<true, false, kBf16Clamp>, grid_for(nblk, di.sms, occ[1]), stream, A);
     } else {
-        swiglu_nvfp4_kernel<false, false, kBf16Clamp>
-            <<<grid_for(nblk, di.sms, occ[0]), kThreads, 0, stream>>>(A);
+        launch(swiglu_nvfp4_kernel<false, false, kBf16Clamp>, grid_for(nblk, di.sms, occ[0]), stream, A);
     }
 }
 
@@ -776,8 +809,8 @@ int moe_nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* pack
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     const int64_t nblk = rows * (K / 16);
-    nvfp4_quantize_kernel<<<grid_for(nblk, di.sms, di.occ_quant, kUnrollQuant), kThreads, 0,
-                            reinterpret_cast<cudaStream_t>(stream)>>>(x, nblk, packed, sf);
+    launch(nvfp4_quantize_kernel, grid_for(nblk, di.sms, di.occ_quant, kUnrollQuant),
+           reinterpret_cast<cudaStream_t>(stream), x, nblk, packed, sf);
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 
@@ -803,8 +836,8 @@ int moe_swiglu_precise_values(const uint16_t* gu, int64_t rows, int64_t I, float
     if (rows == 0) return MOE_NVFP4_OK;
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
-    swiglu_precise_values_kernel<<<di.sms * 8, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        gu, rows, I, clamp_L, y);
+    launch(swiglu_precise_values_kernel, di.sms * 8, reinterpret_cast<cudaStream_t>(stream), gu, rows,
+           I, clamp_L, y);
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 
