@@ -69,6 +69,13 @@ def _load():
         "quantize_element_with_scale": (ctypes.c_uint8, [ctypes.c_float, ctypes.c_uint8]),
         "fp8_e4m3_from_float32_array": (None, [_P, _I64, _P]),
         "quantize_e2m1_nibble_array": (None, [_P, _I64, _P]),
+        "bf16_round": (ctypes.c_float, [ctypes.c_float]),
+        "quantize_nvfp4_scaled": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, _P]),
+        "swiglu_quantize_nvfp4_ex": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P,
+                                                    ctypes.c_int32, _P, _I64, ctypes.c_float,
+                                                    ctypes.c_int, _P, _P]),
+        "swiglu_bf16": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, ctypes.c_int32, _P]),
+        "dequantize_nvfp4": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_float, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -225,3 +232,70 @@ def swiglu_clamped_array(g, u, clamp_L: float) -> np.ndarray:
     y = np.zeros_like(g)
     _load().swiglu_clamped_array(_ptr(g), _ptr(u), g.shape[0], float(clamp_L), _ptr(y))
     return y
+
+
+# ---- extensions: two-level scale, BF16 compat / compact, padded segments,
+#      dequantization (each a reading of the pages; see nvfp4_oracle.c) ----
+
+def bf16_round(v: float) -> float:
+    return float(_load().bf16_round(float(np.float32(v))))
+
+
+def quantize_nvfp4_scaled(x_bf16: np.ndarray, gs: float):
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, K = x.shape
+    packed = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    if _load().quantize_nvfp4_scaled(_ptr(x), rows, K, float(np.float32(gs)), _ptr(packed), _ptr(sf)):
+        raise ValueError("oracle quantize_nvfp4_scaled rejected its arguments")
+    return packed, sf
+
+
+def swiglu_quantize_nvfp4_ex(gu_bf16: np.ndarray, clamp_L: float, offsets=None, out_offsets=None,
+                             out_rows=None, global_scale=1.0, round_bf16=False,
+                             packed=None, sf=None):
+    """The fused step with the extensions; outputs have out_rows rows (the
+    input's row count unless out_offsets is given)."""
+    gu = np.ascontiguousarray(gu_bf16, dtype=np.uint16)
+    rows, two_i = gu.shape
+    I = two_i // 2
+    orows = rows if out_rows is None else int(out_rows)
+    if packed is None:
+        packed = np.zeros((orows, I // 2), np.uint8)
+    if sf is None:
+        sf = np.zeros((orows, I // 16), np.uint8)
+    off = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int32)
+    ooff = None if out_offsets is None else np.ascontiguousarray(out_offsets, dtype=np.int32)
+    E = 0 if off is None else off.shape[0] - 1
+    rc = _load().swiglu_quantize_nvfp4_ex(
+        _ptr(gu), rows, I, float(clamp_L), None if off is None else _ptr(off), E,
+        None if ooff is None else _ptr(ooff), orows, float(np.float32(global_scale)),
+        1 if round_bf16 else 0, _ptr(packed), _ptr(sf))
+    if rc != 0:
+        raise ValueError("oracle swiglu_quantize_nvfp4_ex rejected its arguments")
+    return packed, sf
+
+
+def swiglu_bf16(gu_bf16: np.ndarray, clamp_L: float, offsets=None, out=None):
+    gu = np.ascontiguousarray(gu_bf16, dtype=np.uint16)
+    rows, two_i = gu.shape
+    I = two_i // 2
+    if out is None:
+        out = np.zeros((rows, I), np.uint16)
+    off = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int32)
+    E = 0 if off is None else off.shape[0] - 1
+    if _load().swiglu_bf16(_ptr(gu), rows, I, float(clamp_L), None if off is None else _ptr(off),
+                           E, _ptr(out)):
+        raise ValueError("oracle swiglu_bf16 rejected its arguments")
+    return out
+
+
+def dequantize_nvfp4(packed: np.ndarray, sf: np.ndarray, global_scale=1.0) -> np.ndarray:
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    s = np.ascontiguousarray(sf, dtype=np.uint8)
+    rows, half = p.shape
+    K = 2 * half
+    out = np.zeros((rows, K), np.uint16)
+    if _load().dequantize_nvfp4(_ptr(p), _ptr(s), rows, K, float(np.float32(global_scale)), _ptr(out)):
+        raise ValueError("oracle dequantize_nvfp4 rejected its arguments")
+    return out

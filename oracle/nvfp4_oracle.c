@@ -300,3 +300,120 @@ EXPORT void quantize_e2m1_nibble_array(const float *s, int64_t n, uint8_t *out)
 {
     for (int64_t i = 0; i < n; i++) out[i] = quantize_e2m1_nibble(s[i]);
 }
+
+/* ------------------------------------------------------------------------
+ * Extensions of the step (the pages pass these without defining them; each
+ * definition below is a READING):
+ *  - two-level NVFP4 [P2] (quantize_activation_nvfp4 with a global_scale,
+ *    "l2_global_scale" passed to the epilogue): the FP32 global scale gs
+ *    multiplies every value before the block quantization, v = fl(y * gs);
+ *    dequantization divides by it;
+ *  - the pages' own two-kernel flow [AU]: the L1 epilogue stores the SwiGLU
+ *    as BF16, so y is rounded to BF16 before quantizing ("compat" mode), and
+ *    the compact plan writes that BF16 tensor [rows, I] for a separate
+ *    quantize-only pass;
+ *  - padded per-expert output [AU] ("padded_activated_fp4"): the rows of
+ *    segment e land at output rows out_offsets[e] + (r - offsets[e]);
+ *  - dequantization, the consumer's view: value = e2m1 * e4m3 / gs, rounded
+ *    to BF16.
+ * ------------------------------------------------------------------------ */
+
+/* fp32 -> BF16 value, round to nearest even (finite inputs). */
+EXPORT float bf16_round(float v)
+{
+    uint32_t b = f32_bits(v);
+    uint32_t lsb = (b >> 16) & 1u;
+    b = (b + 0x7fffu + lsb) & 0xffff0000u;
+    return bits_f32(b);
+}
+
+EXPORT int quantize_nvfp4_scaled(const uint16_t *x, int64_t rows, int64_t K, float gs,
+                                 uint8_t *packed, uint8_t *sf)
+{
+    if (rows < 0 || K <= 0 || K % 16 != 0) return -1;
+    float y[16];
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < K / 16; b++) {
+            for (int i = 0; i < 16; i++) y[i] = bf16_to_float32(x[r * K + 16 * b + i]) * gs;
+            quantize_nvfp4_block(y, packed + r * (K / 2) + 8 * b, sf + r * (K / 16) + b);
+        }
+    return 0;
+}
+
+/* The activation value of output column c of input row r, in the given
+ * mode: the fp32 SwiGLU, optionally rounded to BF16, times gs. */
+static float activation_at(const uint16_t *gu, int64_t I, float L, int64_t r, int64_t c,
+                           int round_bf16, float gs)
+{
+    float y = swiglu_at(gu, I, L, r, c);
+    if (round_bf16) y = bf16_round(y);
+    return y * gs;
+}
+
+/*
+ * Fused step with the extensions: rows of segment e (or all rows when
+ * num_experts == 0) are quantized; input row r of segment e is written to
+ * output row out_offsets[e] + (r - offsets[e]) when out_offsets is given
+ * (rows outside [0, out_rows) are skipped), else to row r.
+ */
+EXPORT int swiglu_quantize_nvfp4_ex(const uint16_t *gu, int64_t rows, int64_t I, float L,
+                                    const int32_t *offsets, int32_t num_experts,
+                                    const int32_t *out_offsets, int64_t out_rows,
+                                    float gs, int round_bf16, uint8_t *packed, uint8_t *sf)
+{
+    if (rows < 0 || I <= 0 || I % 16 != 0) return -1;
+    float y[16];
+    int32_t nseg = num_experts > 0 ? num_experts : 1;
+    for (int32_t e = 0; e < nseg; e++) {
+        int64_t r0 = num_experts > 0 ? offsets[e] : 0;
+        int64_t r1 = num_experts > 0 ? offsets[e + 1] : rows;
+        for (int64_t r = r0; r < r1; r++) {
+            if (r < 0 || r >= rows) continue;
+            int64_t ro = r;
+            if (num_experts > 0 && out_offsets != NULL) {
+                ro = out_offsets[e] + (r - r0);
+                if (ro < 0 || ro >= out_rows) continue;
+            }
+            for (int64_t b = 0; b < I / 16; b++) {
+                for (int i = 0; i < 16; i++) y[i] = activation_at(gu, I, L, r, 16 * b + i, round_bf16, gs);
+                quantize_nvfp4_block(y, packed + ro * (I / 2) + 8 * b, sf + ro * (I / 16) + b);
+            }
+        }
+    }
+    return 0;
+}
+
+/* Compact writer: the BF16-rounded SwiGLU of the rows of the segments (or of
+ * all rows), out_bf16 [rows, I] as BF16 bit patterns. */
+EXPORT int swiglu_bf16(const uint16_t *gu, int64_t rows, int64_t I, float L,
+                       const int32_t *offsets, int32_t num_experts, uint16_t *out_bf16)
+{
+    if (rows < 0 || I <= 0 || I % 16 != 0) return -1;
+    int32_t nseg = num_experts > 0 ? num_experts : 1;
+    for (int32_t e = 0; e < nseg; e++) {
+        int64_t r0 = num_experts > 0 ? offsets[e] : 0;
+        int64_t r1 = num_experts > 0 ? offsets[e + 1] : rows;
+        for (int64_t r = r0; r < r1; r++) {
+            if (r < 0 || r >= rows) continue;
+            for (int64_t c = 0; c < I; c++)
+                out_bf16[r * I + c] = (uint16_t)(f32_bits(bf16_round(swiglu_at(gu, I, L, r, c))) >> 16);
+        }
+    }
+    return 0;
+}
+
+/* Dequantization: out_bf16 [rows, K] = RN_bf16((e2m1 value * e4m3 value) / gs). */
+EXPORT int dequantize_nvfp4(const uint8_t *packed, const uint8_t *sf, int64_t rows, int64_t K,
+                            float gs, uint16_t *out_bf16)
+{
+    if (rows < 0 || K <= 0 || K % 16 != 0) return -1;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < K; c++) {
+            uint8_t byte = packed[r * (K / 2) + c / 2];
+            uint8_t nib = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
+            float d = fp8_e4m3_to_float32(sf[r * (K / 16) + c / 16]);
+            float v = (e2m1_nibble_to_float32(nib) * d) / gs;
+            out_bf16[r * K + c] = (uint16_t)(f32_bits(bf16_round(v)) >> 16);
+        }
+    return 0;
+}
