@@ -87,6 +87,7 @@ enum {
     MOE_NVFP4_ECLAMP = -5,      /* clamp_L not finite, not > 0, or > 2^64 */
     MOE_NVFP4_EOFFSETS = -6,    /* num_experts < 0, or offsets NULL with num_experts > 0 */
     MOE_NVFP4_ELAUNCH = -7,     /* the CUDA launch (or a device query) failed */
+    MOE_NVFP4_ESCALE = -8,      /* global_scale not finite, or not > 0 */
 };
 
 /*
@@ -119,6 +120,60 @@ MOE_NVFP4_API int moe_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t K,
 MOE_NVFP4_API int moe_swiglu_nvfp4_quantize(const uint16_t *gu, int64_t rows, int64_t I, float clamp_L,
                               const int32_t *expert_offsets, int32_t num_experts,
                               uint8_t *packed, uint8_t *sf, moe_nvfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Extensions. The pages pass a global scale and use a BF16 intermediate and
+ * padded per-expert rows without defining them ("NVFP4-1.1 Approach, Part 2":
+ * quantize_activation_nvfp4's global_scale, the epilogue's l2_global_scale;
+ * "NVFP4-1.1 Approach Update": the BF16 [gate*8, swiglu*8] store, the compact
+ * BF16 (tokens, I) plan, padded_activated_fp4). The readings implemented:
+ *  - two-level NVFP4: every value is multiplied by the FP32 global scale gs
+ *    (v = fl(value * gs)) and v is quantized as above; dequantization divides
+ *    by gs. Products must not overflow fp32.
+ *  - BF16 compat: the fp32 SwiGLU is rounded to BF16 (RNE) before the
+ *    global scale and the quantization, as the pages' two-kernel flow did;
+ *    the compact writer stores that BF16 tensor [rows, I].
+ *  - padded output: input row r of segment e is written to output row
+ *    out_offsets[e] + (r - offsets[e]); rows of the output not written keep
+ *    their contents; destinations outside [0, out_rows) are skipped.
+ * All are exact (bit-equal to the definitions, like the entry points above).
+ * ------------------------------------------------------------------------- */
+
+typedef struct moe_nvfp4_fused_options {
+    float global_scale;          /* > 0 and finite; 1 = single-level NVFP4 */
+    int32_t round_to_bf16;       /* nonzero: quantize the BF16-rounded SwiGLU */
+    const int32_t *out_offsets;  /* DEVICE int32 [num_experts + 1], or NULL: padded output rows */
+    int64_t out_rows;            /* rows of packed / sf when out_offsets is given */
+} moe_nvfp4_fused_options;
+
+/* Quantize-only with a global scale: x BF16 [rows, K] -> packed [rows, K/2],
+ * sf [rows, K/16] of v = fl(x * global_scale). Same rules as
+ * moe_nvfp4_quantize; MOE_NVFP4_ESCALE for a bad scale. */
+MOE_NVFP4_API int moe_nvfp4_quantize_scaled(const uint16_t *x, int64_t rows, int64_t K,
+                                            float global_scale, uint8_t *packed, uint8_t *sf,
+                                            moe_nvfp4_stream_t stream);
+
+/* The fused step with options (NULL = the plain step). With out_offsets,
+ * packed and sf have out_rows rows and num_experts must be > 0. */
+MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_ex(const uint16_t *gu, int64_t rows, int64_t I,
+                                               float clamp_L, const int32_t *expert_offsets,
+                                               int32_t num_experts,
+                                               const moe_nvfp4_fused_options *options,
+                                               uint8_t *packed, uint8_t *sf,
+                                               moe_nvfp4_stream_t stream);
+
+/* Compact writer: out BF16 [rows, I] (16-byte aligned) = RN_bf16 of the fp32
+ * SwiGLU, for the rows of the segments (others untouched) or all rows. */
+MOE_NVFP4_API int moe_swiglu_bf16(const uint16_t *gu, int64_t rows, int64_t I, float clamp_L,
+                                  const int32_t *expert_offsets, int32_t num_experts,
+                                  uint16_t *out, moe_nvfp4_stream_t stream);
+
+/* Dequantization (the consumer's view): packed [rows, K/2], sf [rows, K/16]
+ * (16-byte aligned) -> out BF16 [rows, K] (32-byte aligned) =
+ * RN_bf16(e2m1 * e4m3 / global_scale); the product is exact in fp32. */
+MOE_NVFP4_API int moe_nvfp4_dequantize(const uint8_t *packed, const uint8_t *sf, int64_t rows,
+                                       int64_t K, float global_scale, uint16_t *out,
+                                       moe_nvfp4_stream_t stream);
 
 /*
  * Diagnostic: the fp32 SwiGLU values y [rows, I] of the fused kernel's fast

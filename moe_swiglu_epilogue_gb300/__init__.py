@@ -17,11 +17,18 @@ import os
 from . import build as _build
 
 __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_values",
-           "moe_swiglu_precise_values",
+           "moe_swiglu_precise_values", "moe_nvfp4_quantize_scaled",
+           "moe_swiglu_nvfp4_quantize_ex", "moe_swiglu_bf16", "moe_nvfp4_dequantize",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
 
 _lib = None
+
+
+class FusedOptions(ctypes.Structure):
+    """moe_nvfp4_fused_options of include/moe_nvfp4.h."""
+    _fields_ = [("global_scale", ctypes.c_float), ("round_to_bf16", ctypes.c_int32),
+                ("out_offsets", ctypes.c_void_p), ("out_rows", ctypes.c_int64)]
 
 
 class MoeNvfp4Error(RuntimeError):
@@ -59,6 +66,15 @@ def load_library():
     lib.moe_swiglu_nvfp4_window.restype = ctypes.c_double
     lib.moe_nvfp4_strerror.argtypes = [ctypes.c_int]
     lib.moe_nvfp4_strerror.restype = ctypes.c_char_p
+    lib.moe_nvfp4_quantize_scaled.argtypes = [P, I64, I64, F, P, P, P]
+    lib.moe_nvfp4_quantize_scaled.restype = ctypes.c_int
+    lib.moe_swiglu_nvfp4_quantize_ex.argtypes = [P, I64, I64, F, P, I32, ctypes.POINTER(FusedOptions),
+                                                 P, P, P]
+    lib.moe_swiglu_nvfp4_quantize_ex.restype = ctypes.c_int
+    lib.moe_swiglu_bf16.argtypes = [P, I64, I64, F, P, I32, P, P]
+    lib.moe_swiglu_bf16.restype = ctypes.c_int
+    lib.moe_nvfp4_dequantize.argtypes = [P, P, I64, I64, F, P, P]
+    lib.moe_nvfp4_dequantize.restype = ctypes.c_int
     lib.moe_nvfp4_abi_version.argtypes = []
     lib.moe_nvfp4_abi_version.restype = ctypes.c_int
     _lib = lib
@@ -212,3 +228,87 @@ def moe_swiglu_precise_values(gu, clamp_L: float, stream=None):
             ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream))
     _check(rc, "moe_swiglu_precise_values")
     return y
+
+
+def moe_nvfp4_quantize_scaled(x, global_scale: float, packed=None, sf=None, stream=None):
+    """Two-level quantize-only: NVFP4 of v = fl(x * global_scale)."""
+    x = _bf16_bits(x, "x", 16)
+    rows, K = x.shape
+    packed = _out(packed, (rows, K // 2), x.device, "packed")
+    sf = _out(sf, (rows, K // 16), x.device, "sf")
+    with _torch().cuda.device(x.device):
+        rc = load_library().moe_nvfp4_quantize_scaled(
+            ctypes.c_void_p(x.data_ptr()), rows, K, float(global_scale),
+            ctypes.c_void_p(packed.data_ptr()), ctypes.c_void_p(sf.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_nvfp4_quantize_scaled")
+    return packed, sf
+
+
+def moe_swiglu_nvfp4_quantize_ex(gu, clamp_L: float, expert_offsets=None, global_scale=1.0,
+                                 round_to_bf16=False, out_offsets=None, out_rows=None,
+                                 packed=None, sf=None, stream=None):
+    """The fused step with a global scale, the BF16-compat mode and padded
+    per-expert output rows (out_offsets: int32 CUDA [E+1], out_rows rows)."""
+    torch = _torch()
+    gu = _bf16_bits(gu, "gu", 32)
+    rows, two_i = gu.shape
+    I = two_i // 2
+    orows = rows
+    ooff_p = None
+    if out_offsets is not None:
+        if out_rows is None:
+            raise ValueError("out_rows is required with out_offsets")
+        if (not out_offsets.is_cuda or out_offsets.dtype != torch.int32
+                or not out_offsets.is_contiguous()):
+            raise ValueError("out_offsets must be a contiguous int32 CUDA tensor")
+        orows = int(out_rows)
+        ooff_p = out_offsets.data_ptr()
+    packed = _out(packed, (orows, I // 2), gu.device, "packed")
+    sf = _out(sf, (orows, I // 16), gu.device, "sf")
+    off_p, E = _offsets_arg(expert_offsets, gu.device)
+    opt = FusedOptions(float(global_scale), 1 if round_to_bf16 else 0, ooff_p, orows)
+    with torch.cuda.device(gu.device):
+        rc = load_library().moe_swiglu_nvfp4_quantize_ex(
+            ctypes.c_void_p(gu.data_ptr()), rows, I, float(clamp_L), off_p, E, ctypes.byref(opt),
+            ctypes.c_void_p(packed.data_ptr()), ctypes.c_void_p(sf.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_swiglu_nvfp4_quantize_ex")
+    return packed, sf
+
+
+def moe_swiglu_bf16(gu, clamp_L: float, expert_offsets=None, out=None, stream=None):
+    """Compact writer: the BF16-rounded SwiGLU [rows, I] (torch.bfloat16)."""
+    torch = _torch()
+    gu = _bf16_bits(gu, "gu", 32)
+    rows, two_i = gu.shape
+    I = two_i // 2
+    if out is None:
+        out = torch.empty((rows, I), dtype=torch.bfloat16, device=gu.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (rows, I) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous bfloat16 tensor of shape {(rows, I)}")
+    off_p, E = _offsets_arg(expert_offsets, gu.device)
+    with torch.cuda.device(gu.device):
+        rc = load_library().moe_swiglu_bf16(
+            ctypes.c_void_p(gu.data_ptr()), rows, I, float(clamp_L), off_p, E,
+            ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_swiglu_bf16")
+    return out
+
+
+def moe_nvfp4_dequantize(packed, sf, global_scale=1.0, out=None, stream=None):
+    """NVFP4 -> BF16 [rows, K]: RN_bf16(e2m1 * e4m3 / global_scale)."""
+    torch = _torch()
+    if packed.dtype != torch.uint8 or sf.dtype != torch.uint8 or packed.dim() != 2 \
+            or not packed.is_cuda or not packed.is_contiguous() or not sf.is_contiguous():
+        raise ValueError("packed and sf must be contiguous uint8 CUDA tensors")
+    rows, half = packed.shape
+    K = 2 * half
+    if tuple(sf.shape) != (rows, K // 16):
+        raise ValueError(f"sf must have shape {(rows, K // 16)}")
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.bfloat16, device=packed.device)
+    with torch.cuda.device(packed.device):
+        rc = load_library().moe_nvfp4_dequantize(
+            ctypes.c_void_p(packed.data_ptr()), ctypes.c_void_p(sf.data_ptr()), rows, K,
+            float(global_scale), ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_nvfp4_dequantize")
+    return out

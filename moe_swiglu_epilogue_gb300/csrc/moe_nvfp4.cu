@@ -146,6 +146,25 @@ __device__ __forceinline__ uint32_t e2m1x8(const float* v) {
     return r;
 }
 
+// Two fp32 -> BF16x2 (RNE): `hi` in bits 16-31, `lo` in 0-15.
+__device__ __forceinline__ uint32_t bf16x2_rn(float hi, float lo) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Byte `k` (0..3) of w, two E2M1 nibbles -> their values as f16x2 (low
+// nibble in the low half).
+template <int k>
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
+    uint32_t h;
+    if (k == 0) asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b0; }" : "=r"(h) : "r"(w));
+    if (k == 1) asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b1; }" : "=r"(h) : "r"(w));
+    if (k == 2) asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b2; }" : "=r"(h) : "r"(w));
+    if (k == 3) asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b3; }" : "=r"(h) : "r"(w));
+    return h;
+}
+
 // ---------------------------------------------------------------------------
 // Scalar pieces
 // ---------------------------------------------------------------------------
@@ -308,9 +327,9 @@ __device__ __forceinline__ DFloat exp_df(float x) {
 }
 
 // The definition's value: silu(min(g, L)) * clamp(u, -L, L) rounded once to
-// fp32, from a double-float evaluation (a gate below -80 falls back to
-// double precision; such an element is far too small to reach any rounding
-// decision, so the fallback only keeps the function total).
+// fp32, from a double-float evaluation (a gate below -80 and results below
+// 2^-100 fall back to double precision: no NVFP4 decision depends on such
+// values, but a BF16 rounding can).
 __device__ __noinline__ float swiglu_precise(float g, float u, float L) {
     const float a = fminf(g, L);
     const float b = fminf(fmaxf(u, -L), L);
@@ -325,6 +344,9 @@ __device__ __noinline__ float swiglu_precise(float g, float u, float L) {
     }
     const DFloat ab = df_two_prod(a, b);
     const DFloat y = df_mul(ab, sig);
+    // near and below the fp32 subnormal range the low parts lose bits:
+    // take the double-precision evaluation there
+    if (fabsf(y.hi) < 0x1p-100f) return swiglu_double(g, u, L);
     return copysignf(y.hi, ab.hi);
 }
 
@@ -343,6 +365,37 @@ __device__ __forceinline__ uint32_t nibble_by_definition(float y, float d, uint3
     const int h = __float2int_rn(fminf(fabsf(s), 6.0f) * 2.0f);
     const uint32_t idx = static_cast<uint32_t>(0x7766665443210ull >> (4 * h)) & 0xFu;
     return idx | ((__float_as_uint(s) >> 28) & 8u);
+}
+
+// Exact NVFP4 quantization of 16 fp32 values (the definition's decisions):
+// amax / 6 correctly rounded (Markstein correction with RN(1/6)), the
+// hardware's RNE + saturating E4M3 cast, the correctly rounded quotient
+// |v| / d by the same correction, the exact half-step rounding, and the
+// hardware E2M1 cast of the signed half step. With kIeeeRcp the reciprocal
+// of d is correctly rounded, which the correction needs for arbitrary fp32
+// v; for BF16-valued v any reciprocal within an ulp works, because the
+// corrected quotient is exact at a tie and elsewhere |v| / d sits at least
+// 2^-13 (relative) away from every half-step boundary. Returns the code.
+template <bool kIeeeRcp>
+__device__ __forceinline__ uint32_t quantize16_exact(const float* v, uint32_t& lo, uint32_t& hi) {
+    const float amax = abs_max16(v);
+    // (scaled values may overflow to inf, which saturates like the definition)
+    const float q = (kIeeeRcp && isinf(amax)) ? amax : div6(amax);
+    const uint32_t code = e4m3x2_rn_sat(0.0f, q) & 0xFFu;
+    const float d = e4m3_value(code);
+    const float inv = (code == 0u) ? 0.0f : (kIeeeRcp ? __frcp_rn(d) : rcp_approx(d));
+    float hs[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const float ax = fabsf(v[i]);
+        const float q0 = ax * inv;
+        float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);           // |v| / d, corrected
+        if (kIeeeRcp && isinf(ax)) q1 = ax;
+        hs[i] = with_sign_of((q1 + kHalfStepBias) - kHalfStepBias, v[i]);
+    }
+    lo = e2m1x8(hs);
+    hi = e2m1x8(hs + 8);
+    return code;
 }
 
 // Half-step index pairs (k, k+1) whose table entries differ, as a bit mask
@@ -563,6 +616,276 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Extensions of the fused step: two-level (global) scale, the pages' BF16
+// pipeline (compat quantize and compact writer), padded per-expert output.
+// A separate kernel, so the plain step above keeps its code as measured.
+// ---------------------------------------------------------------------------
+
+enum ExMode : int { kExQuantize = 0, kExCompat = 1, kExCompact = 2 };
+
+struct ExArgs {
+    FusedArgs f;                    // f.W and its derived fields include the global-scale product
+    float gs;                       // global scale (1: single-level)
+    const int32_t* out_offsets;     // [E+1] or null: padded output rows
+    int64_t out_rows;               // rows of packed / sf
+    uint16_t* out_bf16;             // compact writer output [rows, I]
+    float gate_floor;               // most negative gate the window's bound covers
+};
+
+// Fast SwiGLU of one block's 16 outputs.
+template <bool kBf16Clamp>
+__device__ __forceinline__ void fast_swiglu16(const FusedArgs& A, const uint32_t* w, float* y) {
+    const float L = A.L;
+#pragma unroll
+    for (int grp = 0; grp < 2; grp++) {
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            uint32_t gw = w[8 * grp + p], uw = w[8 * grp + 4 + p];
+            float g0, g1, u0, u1;
+            if (kBf16Clamp) {
+                gw = bf16x2_min(gw, A.L2);
+                uw = bf16x2_min(bf16x2_max(uw, A.negL2), A.L2);
+                g0 = bf16_lo(gw); g1 = bf16_hi(gw);
+                u0 = bf16_lo(uw); u1 = bf16_hi(uw);
+            } else {
+                g0 = fminf(bf16_lo(gw), L); g1 = fminf(bf16_hi(gw), L);
+                u0 = fminf(fmaxf(bf16_lo(uw), -L), L); u1 = fminf(fmaxf(bf16_hi(uw), -L), L);
+            }
+            y[8 * grp + 2 * p] = silu_times_fast(g0, u0);
+            y[8 * grp + 2 * p + 1] = silu_times_fast(g1, u1);
+        }
+    }
+}
+
+// BF16 values of the 16 outputs by the definition (RN_bf16 of the fp32
+// SwiGLU) as 8 BF16x2 words, element 2p in the low half of word p: each pair
+// of fast values is rounded at both ends of the window; when the ends agree
+// that is the definition's rounding, otherwise the pair is re-evaluated
+// (all lanes needing pair q together).
+__device__ __forceinline__ bool outside_window_range(float g, float u, float y, float gate_floor) {
+    // the window bounds the fast path's relative error for gates >=
+    // gate_floor and normal results; a BF16 rounding is scale-free, so any
+    // other nonzero value is redone (a zero gate or up gives an exact +-0)
+    const bool nonzero = (__float_as_uint(g) & 0x7FFFFFFFu) != 0u && (__float_as_uint(u) & 0x7FFFFFFFu) != 0u;
+    return g < gate_floor || (nonzero && fabsf(y) < 0x1p-100f);
+}
+
+__device__ __forceinline__ void bf16_of_block(const FusedArgs& A, const uint16_t* blk_in, bool valid,
+                                              const uint32_t* w, float gate_floor, const float* y,
+                                              uint32_t* yb) {
+    uint32_t amb = 0;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        const uint32_t lo_end = bf16x2_rn(y[2 * q + 1] * A.Wm1, y[2 * q] * A.Wm1);
+        const uint32_t hi_end = bf16x2_rn(y[2 * q + 1] * A.Wp1, y[2 * q] * A.Wp1);
+        yb[q] = lo_end;
+        const int grp = (2 * q) >> 3, pw = ((2 * q) & 7) >> 1;
+        const uint32_t gw = w[8 * grp + pw], uw = w[8 * grp + 4 + pw];
+        const bool odd = outside_window_range(bf16_lo(gw), bf16_lo(uw), y[2 * q], gate_floor) ||
+                         outside_window_range(bf16_hi(gw), bf16_hi(uw), y[2 * q + 1], gate_floor);
+        amb |= (lo_end != hi_end || odd ? 1u : 0u) << q;
+    }
+    if (!valid) amb = 0;
+    if (__any_sync(kFullMask, amb != 0u)) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const bool mine = (amb >> q) & 1u;
+            if (__any_sync(kFullMask, mine) && mine) {
+                float g0, u0, g1, u1;
+                gate_up_at(blk_in, 2 * q, g0, u0);
+                gate_up_at(blk_in, 2 * q + 1, g1, u1);
+                yb[q] = bf16x2_rn(swiglu_precise(g1, u1, A.L), swiglu_precise(g0, u0, A.L));
+            }
+        }
+    }
+}
+
+// The two-level fused step for one block: v = y * gs, then the plain step's
+// fast decisions and exact path on v.
+__device__ __forceinline__ void scaled_block(const ExArgs& X, const uint16_t* blk_in, bool valid,
+                                             const float* y, uint32_t& lo, uint32_t& hi,
+                                             uint32_t& code) {
+    const FusedArgs& A = X.f;
+    const float L = A.L, gs = X.gs;
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = y[i] * gs;
+    const float amax = abs_max16(v);
+    const float q = amax * kInv6;
+    const uint32_t ends = e4m3x2_rn_sat(q * A.Wp1, q * A.Wm1);
+    code = ends & 0xFFu;
+    if (valid && (ends >> 8) != code) {
+        const float lim = amax * (1.0f - 2.0f * A.W);
+        float am = 0.0f;
+        for (int i = 0; i < 16; i++) {
+            if (fabsf(v[i]) >= lim) {
+                float g, u;
+                gate_up_at(blk_in, i, g, u);
+                am = fmaxf(am, fabsf(__fmul_rn(swiglu_precise(g, u, L), gs)));
+            }
+        }
+        code = e4m3x2_rn_sat(0.0f, __fdiv_rn(am, 6.0f)) & 0xFFu;
+    }
+    const float d = e4m3_value(code);
+    const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
+    float hs[16], cl[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const float av = fabsf(v[i]);
+        const float h = fmaf(av, inv, kHalfStepBias) - kHalfStepBias;
+        cl[i] = fmaf(A.W, h, fabsf(fmaf(av, inv, -h)));
+        hs[i] = with_sign_of(h, v[i]);
+    }
+    const float closeness = abs_max16(cl);
+    lo = e2m1x8(hs);
+    hi = e2m1x8(hs + 8);
+    const bool near = valid && closeness > A.near_thr;
+    if (__any_sync(kFullMask, near)) {
+        uint32_t todo = 0;
+        if (near) {
+            for (int i = 0; i < 16; i++) {
+                const float av = fabsf(v[i]);
+                const float h = fmaf(av, inv, kHalfStepBias) - kHalfStepBias;
+                const float rr = fmaf(av, inv, -h);
+                if (fmaf(A.W, h, fabsf(rr)) > A.near_thr) {
+                    const int k = __float2int_rn(2.0f * h) - (rr < 0.0f ? 1 : 0);
+                    if (k >= 0 && k < 12 && ((kNibbleChangingBoundaries >> k) & 1u)) todo |= 1u << i;
+                }
+            }
+        }
+        while (__any_sync(kFullMask, todo != 0u)) {
+            if (todo != 0u) {
+                const int i = __ffs(todo) - 1;
+                todo &= todo - 1u;
+                float g, u;
+                gate_up_at(blk_in, i, g, u);
+                const uint32_t nib =
+                    nibble_by_definition(__fmul_rn(swiglu_precise(g, u, L), gs), d, code);
+                const int sh = 4 * (i & 7);
+                if (i < 8) lo = (lo & ~(0xFu << sh)) | (nib << sh);
+                else       hi = (hi & ~(0xFu << sh)) | (nib << sh);
+            }
+        }
+    }
+}
+
+// Segment of row r: the largest e with offsets[e] <= r (offsets
+// non-decreasing, r inside [offsets[0], offsets[E])).
+__device__ __forceinline__ int segment_of(const int32_t* offsets, int E, int64_t r) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(__ldg(offsets + mid)) <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int kMode, bool kBf16Clamp>
+__global__ void __launch_bounds__(kThreads, kMinBlocksFused)
+swiglu_ex_kernel(const ExArgs X) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const FusedArgs& A = X.f;
+    int64_t b0, b1;
+    active_block_range(A.offsets, A.E, A.rows, A.bpr, b0, b1);
+    const uint64_t pol = l2_evict_first_policy();
+    const int lane = threadIdx.x & 31;
+    constexpr int64_t kChunk = 32 * kUnroll;
+    const int64_t total = b1 - b0;
+    int64_t per_cta = (total + gridDim.x - 1) / gridDim.x;
+    per_cta = (per_cta + kChunk - 1) / kChunk * kChunk;
+    const int64_t cta_begin = b0 + static_cast<int64_t>(blockIdx.x) * per_cta;
+    const int64_t cta_end = cta_begin + per_cta < b1 ? cta_begin + per_cta : b1;
+    const bool padded = (kMode != kExCompact) && X.out_offsets != nullptr && A.offsets != nullptr;
+    __shared__ int next_chunk;
+    if (threadIdx.x == 0) next_chunk = 0;
+    __syncthreads();
+    for (;;) {                                              // warp-uniform
+        int c = 0;
+        if (lane == 0) c = atomicAdd(&next_chunk, 1);
+        c = __shfl_sync(kFullMask, c, 0);
+        const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
+        if (base >= cta_end) break;
+        // padded output: the chunk's first row, its column and its segment
+        int64_t r0 = 0, c0 = 0;
+        int e0 = 0;
+        if (padded) {
+            if (lane == 0) {
+                r0 = base / A.bpr;
+                c0 = base - r0 * A.bpr;
+                e0 = segment_of(A.offsets, A.E, r0);
+            }
+            r0 = __shfl_sync(kFullMask, r0, 0);
+            c0 = __shfl_sync(kFullMask, c0, 0);
+            e0 = __shfl_sync(kFullMask, e0, 0);
+        }
+        uint32_t w[kUnroll][16];
+#pragma unroll
+        for (int k = 0; k < kUnroll; k++) {
+            const int64_t blk = base + 32 * k + lane;
+            if (blk < cta_end) {
+                const uint16_t* p = A.gu + blk * 32;
+                load_stream_32B(p, pol, w[k]);
+                load_stream_32B(p + 16, pol, w[k] + 8);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) w[k][j] = 0u;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; k++) {
+            const int64_t blk = base + 32 * k + lane;
+            const bool valid = blk < cta_end;
+            int64_t oblk = blk;
+            bool store = valid;
+            if (padded && valid) {
+                const int64_t j = c0 + 32 * k + lane;
+                const int64_t row = r0 + (A.bpr >= kChunk ? (j >= A.bpr ? 1 : 0) : j / A.bpr);
+                int e = e0;
+                while (e + 1 < A.E && row >= static_cast<int64_t>(__ldg(A.offsets + e + 1))) e++;
+                const int64_t orow = __ldg(X.out_offsets + e) + (row - __ldg(A.offsets + e));
+                store = orow >= 0 && orow < X.out_rows;
+                oblk = orow * A.bpr + (blk - row * A.bpr);
+            }
+            const uint16_t* blk_in = A.gu + blk * 32;
+            float y[16];
+            fast_swiglu16<kBf16Clamp>(A, w[k], y);
+            if (kMode == kExQuantize) {
+                uint32_t lo, hi, code;
+                scaled_block(X, blk_in, valid, y, lo, hi, code);
+                if (store) {
+                    *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
+                    A.sf[oblk] = static_cast<uint8_t>(code);
+                }
+            } else {
+                uint32_t yb[8];
+                bf16_of_block(A, blk_in, valid, w[k], X.gate_floor, y, yb);
+                if (kMode == kExCompact) {
+                    if (store) {
+                        uint4* dst = reinterpret_cast<uint4*>(X.out_bf16 + blk * 16);
+                        dst[0] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+                        dst[1] = make_uint4(yb[4], yb[5], yb[6], yb[7]);
+                    }
+                } else {                                // compat: quantize the BF16 values
+                    float v[16];
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        v[2 * q] = __fmul_rn(bf16_lo(yb[q]), X.gs);
+                        v[2 * q + 1] = __fmul_rn(bf16_hi(yb[q]), X.gs);
+                    }
+                    uint32_t lo, hi;
+                    const uint32_t code = quantize16_exact<true>(v, lo, hi);
+                    if (store) {
+                        *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
+                        A.sf[oblk] = static_cast<uint8_t>(code);
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Diagnostic: the definition-path SwiGLU value of every output element.
 __global__ void swiglu_precise_values_kernel(const uint16_t* __restrict__ gu, int64_t rows,
                                              int64_t I, float L, float* __restrict__ y) {
@@ -584,8 +907,9 @@ __global__ void swiglu_precise_values_kernel(const uint16_t* __restrict__ gu, in
 // Quantize-only
 // ---------------------------------------------------------------------------
 
+template <bool kScaled>
 __global__ void __launch_bounds__(kThreads, kMinBlocksQuant)
-nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk,
+nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
                       uint8_t* __restrict__ packed, uint8_t* __restrict__ sf) {
     wait_for_preceding_grid();
     allow_next_grid_launch();
@@ -606,24 +930,51 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk,
             if (blk >= nblk) continue;
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; i++) v[i] = (i & 1) ? bf16_hi(w[k][i >> 1]) : bf16_lo(w[k][i >> 1]);
-            const uint32_t code = e4m3x2_rn_sat(0.0f, div6(abs_max16(v))) & 0xFFu;
-            const float d = e4m3_value(code);
-            // any reciprocal within an ulp works: the corrected quotient
-            // below is exact at a tie, and elsewhere |x| / d sits at least
-            // 2^-13 (relative) away from every half-step boundary
-            const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
-            float hs[16];
-#pragma unroll
             for (int i = 0; i < 16; i++) {
-                const float ax = fabsf(v[i]);
-                const float q0 = ax * inv;
-                const float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);     // |x| / d, corrected
-                hs[i] = with_sign_of((q1 + kHalfStepBias) - kHalfStepBias, v[i]);
+                v[i] = (i & 1) ? bf16_hi(w[k][i >> 1]) : bf16_lo(w[k][i >> 1]);
+                if (kScaled) v[i] = __fmul_rn(v[i], gs);          // two-level: v = fl(x * gs)
             }
-            *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(e2m1x8(hs), e2m1x8(hs + 8));
+            uint32_t lo, hi;
+            const uint32_t code = quantize16_exact<kScaled>(v, lo, hi);
+            *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(lo, hi);
             sf[blk] = static_cast<uint8_t>(code);
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantization: NVFP4 -> BF16, value = e2m1 * e4m3 / gs
+// ---------------------------------------------------------------------------
+
+template <bool kScaled>
+__global__ void __launch_bounds__(kThreads)
+nvfp4_dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ sf,
+                        int64_t nblk, float gs, uint16_t* __restrict__ out) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; blk < nblk;
+         blk += stride) {
+        const uint2 p = *reinterpret_cast<const uint2*>(packed + blk * 8);
+        const float d = e4m3_value(sf[blk]);
+        uint32_t o[8];
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+            const uint32_t w = half ? p.y : p.x;
+            const uint32_t h2[4] = {e2m1x2_to_f16x2<0>(w), e2m1x2_to_f16x2<1>(w),
+                                    e2m1x2_to_f16x2<2>(w), e2m1x2_to_f16x2<3>(w)};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                // e2m1 * e4m3 is exact in fp32 (at most 6 significant bits)
+                float a = __half2float(__ushort_as_half(static_cast<uint16_t>(h2[k] & 0xFFFFu))) * d;
+                float b = __half2float(__ushort_as_half(static_cast<uint16_t>(h2[k] >> 16))) * d;
+                if (kScaled) { a = __fdiv_rn(a, gs); b = __fdiv_rn(b, gs); }
+                o[4 * half + k] = bf16x2_rn(b, a);
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + blk * 16);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -635,7 +986,8 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};   // [bf16 clamp][plain, counted, values]
-    int occ_quant = 0;
+    int occ_ex[2][3] = {{0, 0, 0}, {0, 0, 0}};  // [bf16 clamp][ExMode]
+    int occ_quant[2] = {0, 0};                  // [scaled]
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -650,6 +1002,16 @@ bool fused_occupancy(int* occ) {
                &occ[2], swiglu_nvfp4_kernel<false, true, kBf16Clamp>, kThreads, 0) == cudaSuccess;
 }
 
+template <bool kBf16Clamp>
+bool ex_occupancy(int* occ) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[0], swiglu_ex_kernel<kExQuantize, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[1], swiglu_ex_kernel<kExCompat, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[2], swiglu_ex_kernel<kExCompact, kBf16Clamp>, kThreads, 0) == cudaSuccess;
+}
+
 int device_info(DeviceInfo& out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_NVFP4_ELAUNCH;
@@ -659,8 +1021,11 @@ int device_info(DeviceInfo& out) {
         if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
         if (!fused_occupancy<false>(di.occ[0]) || !fused_occupancy<true>(di.occ[1]) ||
+            !ex_occupancy<false>(di.occ_ex[0]) || !ex_occupancy<true>(di.occ_ex[1]) ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &di.occ_quant, nvfp4_quantize_kernel, kThreads, 0) != cudaSuccess)
+                &di.occ_quant[0], nvfp4_quantize_kernel<false>, kThreads, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &di.occ_quant[1], nvfp4_quantize_kernel<true>, kThreads, 0) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
         di.ready = true;
     }
@@ -695,6 +1060,21 @@ int check_common(const void* in, int64_t rows, int64_t width, int64_t in_bytes_p
 // test suite measures it exhaustively on the GPU and checks this bound).
 constexpr double kFastSiluMaxRelErr = 8.5e-7;
 constexpr double kFastSiluGateFloor = -16.0;
+
+// The most negative gate for which window_for(L) bounds the fast error.
+double window_gate_floor(float L) {
+    const double target = std::ldexp(1.0, -12) / static_cast<double>(L);
+    double z = 1.0;
+    if (target < std::exp(-1.0)) {
+        double lo = 1.0, hi = 200.0;
+        for (int it = 0; it < 200; it++) {
+            const double mid = 0.5 * (lo + hi);
+            if (mid * std::exp(-mid) >= target) lo = mid; else hi = mid;
+        }
+        z = hi;
+    }
+    return -z >= kFastSiluGateFloor ? kFastSiluGateFloor : -z;
+}
 
 double window_for(float L) {
     if (!std::isfinite(L) || !(L > 0.0f) || static_cast<double>(L) > 18446744073709551616.0) return -1.0;
@@ -766,6 +1146,70 @@ void launch_fused_kernel(const FusedArgs& A, int64_t nblk, const DeviceInfo& di,
     }
 }
 
+bool valid_scale(float gs) { return std::isfinite(gs) && gs > 0.0f; }
+
+// Fills the fused-step arguments for clamp L and window W.
+FusedArgs fused_args(const uint16_t* gu, int64_t rows, int64_t I, float L, double W,
+                     const int32_t* offsets, int32_t E, uint8_t* packed, uint8_t* sf) {
+    FusedArgs A;
+    A.gu = gu; A.rows = rows; A.bpr = I / 16; A.L = L;
+    const int64_t lb = bf16_bits_of(L);
+    const int64_t nlb = bf16_bits_of(-L);
+    A.L2 = lb < 0 ? 0u : static_cast<uint32_t>(lb) * 0x00010001u;
+    A.negL2 = nlb < 0 ? 0u : static_cast<uint32_t>(nlb) * 0x00010001u;
+    A.W = static_cast<float>(W);
+    A.Wp1 = static_cast<float>(1.0 + W);
+    A.Wm1 = static_cast<float>(1.0 - W);
+    A.near_thr = static_cast<float>(0.25 * (1.0 - W));
+    A.offsets = (E > 0) ? offsets : nullptr; A.E = E;
+    A.packed = packed; A.sf = sf;
+    A.counters = nullptr; A.values = nullptr;
+    return A;
+}
+
+template <bool kBf16Clamp>
+void launch_ex_kernel(const ExArgs& X, int mode, int64_t nblk, const DeviceInfo& di,
+                      cudaStream_t stream) {
+    const int* occ = di.occ_ex[kBf16Clamp ? 1 : 0];
+    if (mode == kExQuantize)
+        launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp>, grid_for(nblk, di.sms, occ[0]), stream, X);
+    else if (mode == kExCompat)
+        launch(swiglu_ex_kernel<kExCompat, kBf16Clamp>, grid_for(nblk, di.sms, occ[1]), stream, X);
+    else
+        launch(swiglu_ex_kernel<kExCompact, kBf16Clamp>, grid_for(nblk, di.sms, occ[2]), stream, X);
+}
+
+int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_t* offsets,
+              int32_t E, float gs, int mode, const int32_t* out_offsets, int64_t out_rows,
+              uint8_t* packed, uint8_t* sf, uint16_t* out_bf16, cudaStream_t stream) {
+    int rc;
+    if (mode == kExCompact) rc = check_common(gu, rows, I, 4, out_bf16, out_bf16);
+    else rc = check_common(gu, rows, I, 4, packed, sf);
+    if (rc != MOE_NVFP4_OK) return rc;
+    double W = window_for(L);
+    if (W < 0.0) return MOE_NVFP4_ECLAMP;
+    if (!valid_scale(gs)) return MOE_NVFP4_ESCALE;
+    if (E < 0 || (E > 0 && offsets == nullptr)) return MOE_NVFP4_EOFFSETS;
+    if (out_offsets != nullptr && E == 0) return MOE_NVFP4_EOFFSETS;
+    if (out_offsets != nullptr && out_rows < 0) return MOE_NVFP4_ESIZE;
+    if (rows == 0) return MOE_NVFP4_OK;
+    DeviceInfo di;
+    if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    // the product with gs rounds once on each side of the comparison
+    W += 1.5 * 2.0 * std::ldexp(1.0, -24);
+    ExArgs X;
+    X.f = fused_args(gu, rows, I, L, W, offsets, E, packed, sf);
+    X.gs = gs;
+    X.out_offsets = (mode == kExCompact) ? nullptr : out_offsets;
+    X.out_rows = out_offsets != nullptr ? out_rows : rows;
+    X.out_bf16 = out_bf16;
+    X.gate_floor = static_cast<float>(window_gate_floor(L));
+    const int64_t nblk = rows * (I / 16);
+    if (bf16_bits_of(L) >= 0) launch_ex_kernel<true>(X, mode, nblk, di, stream);
+    else launch_ex_kernel<false>(X, mode, nblk, di, stream);
+    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+}
+
 int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_t* offsets,
                  int32_t E, uint8_t* packed, uint8_t* sf, uint64_t* counters, float* values,
                  cudaStream_t stream) {
@@ -809,8 +1253,8 @@ int moe_nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* pack
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     const int64_t nblk = rows * (K / 16);
-    launch(nvfp4_quantize_kernel, grid_for(nblk, di.sms, di.occ_quant, kUnrollQuant),
-           reinterpret_cast<cudaStream_t>(stream), x, nblk, packed, sf);
+    launch(nvfp4_quantize_kernel<false>, grid_for(nblk, di.sms, di.occ_quant[0], kUnrollQuant),
+           reinterpret_cast<cudaStream_t>(stream), x, nblk, 1.0f, packed, sf);
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 
@@ -851,6 +1295,62 @@ int moe_swiglu_nvfp4_quantize_counted(const uint16_t* gu, int64_t rows, int64_t 
                         nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int moe_nvfp4_quantize_scaled(const uint16_t* x, int64_t rows, int64_t K, float global_scale,
+                              uint8_t* packed, uint8_t* sf, moe_nvfp4_stream_t stream) {
+    int rc = check_common(x, rows, K, 2, packed, sf);
+    if (rc != MOE_NVFP4_OK) return rc;
+    if (!valid_scale(global_scale)) return MOE_NVFP4_ESCALE;
+    if (rows == 0) return MOE_NVFP4_OK;
+    DeviceInfo di;
+    if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    const int64_t nblk = rows * (K / 16);
+    launch(nvfp4_quantize_kernel<true>, grid_for(nblk, di.sms, di.occ_quant[1], kUnrollQuant),
+           reinterpret_cast<cudaStream_t>(stream), x, nblk, global_scale, packed, sf);
+    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+}
+
+int moe_swiglu_nvfp4_quantize_ex(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
+                                 const int32_t* expert_offsets, int32_t num_experts,
+                                 const moe_nvfp4_fused_options* options, uint8_t* packed,
+                                 uint8_t* sf, moe_nvfp4_stream_t stream) {
+    moe_nvfp4_fused_options opt = {1.0f, 0, nullptr, 0};
+    if (options != nullptr) opt = *options;
+    return launch_ex(gu, rows, I, clamp_L, expert_offsets, num_experts, opt.global_scale,
+                     opt.round_to_bf16 ? kExCompat : kExQuantize, opt.out_offsets, opt.out_rows,
+                     packed, sf, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_swiglu_bf16(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
+                    const int32_t* expert_offsets, int32_t num_experts, uint16_t* out,
+                    moe_nvfp4_stream_t stream) {
+    return launch_ex(gu, rows, I, clamp_L, expert_offsets, num_experts, 1.0f, kExCompact, nullptr,
+                     0, nullptr, nullptr, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_nvfp4_dequantize(const uint8_t* packed, const uint8_t* sf, int64_t rows, int64_t K,
+                         float global_scale, uint16_t* out, moe_nvfp4_stream_t stream) {
+    if (rows < 0) return MOE_NVFP4_ESIZE;
+    if (K <= 0 || K % 16 != 0) return MOE_NVFP4_EWIDTH;
+    if (rows > 0 && K > INT64_MAX / 2 / rows) return MOE_NVFP4_ESIZE;
+    if (!valid_scale(global_scale)) return MOE_NVFP4_ESCALE;
+    if (rows == 0) return MOE_NVFP4_OK;
+    if (packed == nullptr || sf == nullptr || out == nullptr) return MOE_NVFP4_ENULL;
+    if (!aligned(packed, 16) || !aligned(sf, 16) || !aligned(out, 32)) return MOE_NVFP4_EALIGN;
+    DeviceInfo di;
+    int rc = device_info(di);
+    if (rc != MOE_NVFP4_OK) return rc;
+    const int64_t nblk = rows * (K / 16);
+    int64_t grid = (nblk + kThreads - 1) / kThreads;
+    if (grid > static_cast<int64_t>(di.sms) * 8) grid = static_cast<int64_t>(di.sms) * 8;
+    if (global_scale == 1.0f)
+        launch(nvfp4_dequantize_kernel<false>, static_cast<int>(grid),
+               reinterpret_cast<cudaStream_t>(stream), packed, sf, nblk, global_scale, out);
+    else
+        launch(nvfp4_dequantize_kernel<true>, static_cast<int>(grid),
+               reinterpret_cast<cudaStream_t>(stream), packed, sf, nblk, global_scale, out);
+    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+}
+
 double moe_swiglu_nvfp4_window(float clamp_L) { return window_for(clamp_L); }
 
 const char* moe_nvfp4_strerror(int code) {
@@ -863,10 +1363,11 @@ const char* moe_nvfp4_strerror(int code) {
         case MOE_NVFP4_ECLAMP: return "clamp_L must be finite and in (0, 2^64]";
         case MOE_NVFP4_EOFFSETS: return "num_experts < 0, or expert offsets missing";
         case MOE_NVFP4_ELAUNCH: return "CUDA launch or device query failed";
+        case MOE_NVFP4_ESCALE: return "global_scale must be finite and > 0";
         default: return "unknown error code";
     }
 }
 
-int moe_nvfp4_abi_version(void) { return 1; }
+int moe_nvfp4_abi_version(void) { return 2; }
 
 }  // extern "C"

@@ -45,8 +45,8 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.moe_nvfp4_abi_version() == 1
-    for code in range(0, -8, -1):
+    assert lib.moe_nvfp4_abi_version() == 2
+    for code in range(0, -9, -1):
         assert lib.moe_nvfp4_strerror(code)
     assert b"unknown" in lib.moe_nvfp4_strerror(-99)
 
@@ -92,3 +92,31 @@ def test_window(lib):
     assert w7 <= w10 <= lib.moe_swiglu_nvfp4_window(1e6)
     assert lib.moe_swiglu_nvfp4_window(-1.0) < 0
     assert lib.moe_swiglu_nvfp4_window(float("nan")) < 0
+
+
+def test_extension_argument_errors(lib):
+    from moe_swiglu_epilogue_gb300 import FusedOptions
+    import ctypes as C
+    qs = lib.moe_nvfp4_quantize_scaled
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert qs(A32, 0, 32, bad, A16, A16, S) == -8
+    assert qs(A32, 4, 24, 1.0, A16, A16, S) == -2
+    assert qs(A32, 0, 32, 2.0, A16, A16, S) == 0
+    ex = lib.moe_swiglu_nvfp4_quantize_ex
+    opt = FusedOptions(0.0, 0, None, 0)
+    assert ex(A32, 0, 32, 7.0, NULL, 0, C.byref(opt), A16, A16, S) == -8
+    opt = FusedOptions(1.0, 1, 0x7f0000000100, 10)          # padded output without segments
+    assert ex(A32, 0, 32, 7.0, NULL, 0, C.byref(opt), A16, A16, S) == -6
+    opt = FusedOptions(1.0, 0, 0x7f0000000100, -1)
+    assert ex(A32, 0, 32, 7.0, A16, 2, C.byref(opt), A16, A16, S) == -4
+    assert ex(A32, 0, 32, 7.0, NULL, 0, None, A16, A16, S) == 0
+    assert ex(A32, 4, 32, 0.0, NULL, 0, None, A16, A16, S) == -5
+    cw = lib.moe_swiglu_bf16
+    assert cw(A32, 4, 32, 7.0, NULL, 0, NULL, S) == -1
+    assert cw(A32, 4, 32, 7.0, NULL, 0, A2, S) == -3
+    dq = lib.moe_nvfp4_dequantize
+    assert dq(A16, A16, 4, 24, 1.0, A32, S) == -2
+    assert dq(A16, A16, 4, 32, 0.0, A32, S) == -8
+    assert dq(A16, A16, 4, 32, 1.0, A16, S) == -3      # output must be 32-byte aligned
+    assert dq(NULL, A16, 4, 32, 1.0, A32, S) == -1
+    assert dq(NULL, NULL, 0, 32, 1.0, NULL, S) == 0

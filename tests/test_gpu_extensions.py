@@ -1,0 +1,165 @@
+"""GPU parity of the extensions (two-level scale, BF16 compat, compact
+writer, padded per-expert rows, dequantization) with the oracle, through the
+C ABI. All are exact definitions, so every comparison is bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_swiglu_epilogue_gb300 as M
+from moe_swiglu_epilogue_gb300 import workloads as W
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from moe_swiglu_epilogue_gb300 import build
+    build.build()
+    oracle.build()
+    M.load_library()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def bits(t):
+    torch.cuda.synchronize()
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+GS = (1.0, 0.37109375, 3.3, 448.0 * 6.0 / 71.5)
+
+
+@pytest.mark.parametrize("gs", GS)
+def test_quantize_scaled_bit_exact(gs):
+    for w in (W.quantize_normal(rows=256, K=2048, seed=11),
+              W.prefill_heavy_tail_quantize(rows=512, K=1024)):
+        p, s = M.moe_nvfp4_quantize_scaled(dev(w.data), gs)
+        rp, rs = oracle.quantize_nvfp4_scaled(w.data, gs)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+
+
+def test_quantize_scaled_edge_blocks_bit_exact():
+    rng = np.random.default_rng(51)
+    x = parity.quantize_edge_blocks(rng, 12000).reshape(-1, 256)
+    for gs in (0.5, 0.7, 1.3):
+        p, s = M.moe_nvfp4_quantize_scaled(dev(x), gs)
+        rp, rs = oracle.quantize_nvfp4_scaled(x, gs)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+
+
+@pytest.mark.parametrize("gs", GS)
+@pytest.mark.parametrize("compat", [False, True])
+def test_fused_ex_bit_exact(gs, compat):
+    w = W.fused_normal(rows=256, I=2048, seed=3)
+    p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(w.data), w.clamp_L, global_scale=gs,
+                                         round_to_bf16=compat)
+    rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, w.clamp_L, global_scale=gs, round_bf16=compat)
+    assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+
+
+def test_fused_ex_defaults_equal_the_plain_step():
+    w = W.prefill_heavy_tail(rows=256, I=3072)
+    p1, s1 = M.moe_swiglu_nvfp4_quantize_ex(dev(w.data), w.clamp_L)
+    p2, s2 = M.moe_swiglu_nvfp4_quantize(dev(w.data), w.clamp_L)
+    assert torch.equal(p1, p2) and torch.equal(s1, s2)
+
+
+def test_fused_ex_near_tie_blocks_bit_exact():
+    rng = np.random.default_rng(78)
+    blocks, _ = parity.fused_near_tie_blocks(rng, 1024, 7.0)
+    gu = blocks.reshape(-1, 8 * 32)                       # I = 128
+    for gs, compat in ((1.0, True), (0.8125, False), (2.5, True)):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(gu), 7.0, global_scale=gs, round_to_bf16=compat)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(gu, 7.0, global_scale=gs, round_bf16=compat)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+
+
+@pytest.mark.parametrize("I", [64, 2048])
+def test_padded_segments_bit_exact_and_gaps_untouched(I):
+    w = W.ragged_routing(tokens=256, experts=16, topk=4, I=I, pad_rows=9)
+    counts = np.diff(w.offsets)
+    tile = 128
+    padded = np.ceil(counts / tile).astype(np.int64) * tile
+    out_off = np.concatenate([[0], np.cumsum(padded)]).astype(np.int32)
+    out_rows = int(out_off[-1])
+    for gs, compat in ((1.0, False), (1.7, True)):
+        sent_p = np.full((out_rows, I // 2), 0xA5, np.uint8)
+        sent_s = np.full((out_rows, I // 16), 0x5A, np.uint8)
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(
+            dev(w.data), w.clamp_L, torch.from_numpy(w.offsets).cuda(), gs, compat,
+            torch.from_numpy(out_off).cuda(), out_rows, torch.from_numpy(sent_p.copy()).cuda(),
+            torch.from_numpy(sent_s.copy()).cuda())
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, w.clamp_L, w.offsets, out_off, out_rows,
+                                                 gs, compat, packed=sent_p, sf=sent_s)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+        assert np.any(rp == 0xA5)                          # gaps exist and stayed
+
+
+def test_compact_writer_bit_exact():
+    for w in (W.fused_normal(rows=512, I=2048, seed=4), W.prefill_heavy_tail(rows=256, I=3072),
+              W.edge_structured(rows=128, I=4096)):
+        out = M.moe_swiglu_bf16(dev(w.data), w.clamp_L)
+        assert np.array_equal(bits(out), oracle.swiglu_bf16(w.data, w.clamp_L))
+
+
+def test_compact_writer_ragged_rows_untouched():
+    w = W.ragged_routing(tokens=128, experts=8, topk=4, I=256, pad_rows=13)
+    sent = torch.full((w.rows, w.width), 3.0, dtype=torch.bfloat16, device="cuda")
+    out = M.moe_swiglu_bf16(dev(w.data), w.clamp_L, torch.from_numpy(w.offsets).cuda(), sent)
+    ref = oracle.swiglu_bf16(w.data, w.clamp_L, w.offsets,
+                             out=np.full((w.rows, w.width), 0x4040, np.uint16))
+    assert np.array_equal(bits(out), ref)
+
+
+def test_compact_then_quantize_equals_compat():
+    w = W.fused_normal(rows=256, I=1024, seed=8)
+    compact = M.moe_swiglu_bf16(dev(w.data), w.clamp_L)
+    p1, s1 = M.moe_nvfp4_quantize(compact)
+    p2, s2 = M.moe_swiglu_nvfp4_quantize_ex(dev(w.data), w.clamp_L, round_to_bf16=True)
+    assert torch.equal(p1, p2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("gs", [1.0, 2.7, 0.3])
+def test_dequantize_bit_exact_and_round_trip(gs):
+    w = W.quantize_normal(rows=128, K=2048, seed=2)
+    p, s = M.moe_nvfp4_quantize_scaled(dev(w.data), gs)
+    out = M.moe_nvfp4_dequantize(p, s, gs)
+    ref = oracle.dequantize_nvfp4(host(p), host(s), gs)
+    assert np.array_equal(bits(out), ref)
+    # every (nibble, scale) pair
+    codes = np.arange(0x7f, dtype=np.uint8)
+    nibs = np.arange(16, dtype=np.uint8)
+    packed = np.tile((nibs[0::2] | (nibs[1::2] << 4))[None, :], (codes.size + 1, 1))
+    sf = np.concatenate([codes, np.zeros(1, np.uint8)])[:, None]
+    out = M.moe_nvfp4_dequantize(torch.from_numpy(packed).cuda(), torch.from_numpy(sf).cuda(), gs)
+    assert np.array_equal(bits(out), oracle.dequantize_nvfp4(packed, sf, gs))
+
+
+@pytest.mark.parametrize("name", ["ragged", "prefill"])
+def test_full_size_compat_and_compact_sampled(name):
+    w = W.make(name)
+    off = None if w.offsets is None else torch.from_numpy(w.offsets).cuda()
+    g = dev(w.data)
+    p, s = M.moe_swiglu_nvfp4_quantize_ex(g, w.clamp_L, off, 1.25, True)
+    out = M.moe_swiglu_bf16(g, w.clamp_L, off)
+    hp, hs, hb = host(p), host(s), bits(out)
+    rng = np.random.default_rng(1)
+    r0 = 0 if w.offsets is None else int(w.offsets[0])
+    r1 = w.rows if w.offsets is None else int(w.offsets[-1])
+    rows = rng.integers(r0, r1, 24)
+    sub = w.data[rows]
+    rp, rs = oracle.swiglu_quantize_nvfp4_ex(sub, w.clamp_L, global_scale=1.25, round_bf16=True)
+    assert np.array_equal(hs[rows], rs) and np.array_equal(hp[rows], rp)
+    assert np.array_equal(hb[rows], oracle.swiglu_bf16(sub, w.clamp_L))
