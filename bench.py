@@ -359,6 +359,93 @@ def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str
             "timing": "mean launch = timed region / launches (back-to-back on one stream)"}
 
 
+def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, peak: float):
+    """Launch time and algorithmic GB/s of the extensions on the ragged
+    workload (dequantization on the prefill quantize-only outputs): the
+    two-level scale, the BF16-compat mode, padded per-expert output (segments
+    padded to 128 rows), the compact BF16 writer, the compact flow (writer +
+    quantize-only of its output, the pages' planned pipeline) and
+    dequantization."""
+    P = ctypes.c_void_p
+    FO = M.FusedOptions
+    w = W.make("ragged")
+    rows, I, L = w.rows, w.width, w.clamp_L
+    s = P(stream.cuda_stream)
+    srcs = [torch.from_numpy(w.data.view(np.int16)).cuda() for _ in range(2)]
+    off = torch.from_numpy(w.offsets).cuda()
+    E = off.shape[0] - 1
+    packed = torch.empty((rows, I // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((rows, I // 16), dtype=torch.uint8, device="cuda")
+    compact = torch.empty((rows, I), dtype=torch.bfloat16, device="cuda")
+    counts = np.diff(w.offsets)
+    out_off = np.concatenate([[0], np.cumsum(np.ceil(counts / 128).astype(np.int64) * 128)])
+    out_rows = int(out_off[-1])
+    out_off_t = torch.from_numpy(out_off.astype(np.int32)).cuda()
+    packed_p = torch.empty((out_rows, I // 2), dtype=torch.uint8, device="cuda")
+    sf_p = torch.empty((out_rows, I // 16), dtype=torch.uint8, device="cuda")
+    opts = {
+        "two_level_scale": FO(1.25, 0, None, rows),
+        "bf16_compat": FO(1.0, 1, None, rows),
+        "padded_segments": FO(1.0, 0, out_off_t.data_ptr(), out_rows),
+    }
+    fused_bytes = w.algorithmic_bytes()
+    writer_bytes = w.active_rows * (4 * I + 2 * I)
+    quant_bytes = rows * (2 * I + I // 2 + I // 16)
+    res = {}
+
+    def measure(name, calls, nbytes, note):
+        with torch.cuda.stream(stream):
+            tot, per, _, _ = time_steps(torch, calls, steps, warmup, stream)
+        mean_s = statistics.fmean(per)
+        res[name] = {"launch_us_mean": round(mean_s * 1e6, 2),
+                     "gbs": round(nbytes / mean_s / 1e9, 1),
+                     "frac_of_peak": round(nbytes / mean_s / 1e9 / peak, 4), "bytes": nbytes,
+                     "what": note}
+
+    for name, opt in opts.items():
+        pk, sc = (packed_p, sf_p) if name == "padded_segments" else (packed, sf)
+        calls = [DirectCall(lib.moe_swiglu_nvfp4_quantize_ex,
+                            (P(x.data_ptr()), rows, I, ctypes.c_float(L), P(off.data_ptr()),
+                             ctypes.c_int32(E), ctypes.byref(opt), P(pk.data_ptr()),
+                             P(sc.data_ptr()), s)) for x in srcs]
+        measure(name, calls, fused_bytes, "moe_swiglu_nvfp4_quantize_ex on the ragged workload")
+    writer = [DirectCall(lib.moe_swiglu_bf16, (P(x.data_ptr()), rows, I, ctypes.c_float(L),
+                                               P(off.data_ptr()), ctypes.c_int32(E),
+                                               P(compact.data_ptr()), s)) for x in srcs]
+    measure("compact_writer", writer, writer_bytes, "moe_swiglu_bf16: gate/up -> BF16 [rows, I]")
+    quant = DirectCall(lib.moe_nvfp4_quantize, (P(compact.data_ptr()), rows, I,
+                                                P(packed.data_ptr()), P(sf.data_ptr()), s))
+    measure("quantize_of_compact", [quant], quant_bytes, "moe_nvfp4_quantize of the BF16 tensor")
+
+    class Both:
+        def __init__(self, a):
+            self.a = a
+
+        def __call__(self):
+            self.a()
+            quant()
+
+    measure("compact_flow", [Both(c) for c in writer], writer_bytes + quant_bytes,
+            "compact writer + quantize-only per step (bytes: both kernels)")
+    res["compact_flow"]["vs_fused_time"] = None
+    del srcs, compact
+    torch.cuda.empty_cache()
+    wq = W.make("prefill_quantize")
+    x = torch.from_numpy(wq.data.view(np.int16)).cuda()
+    pq = torch.empty((wq.rows, wq.width // 2), dtype=torch.uint8, device="cuda")
+    sq = torch.empty((wq.rows, wq.width // 16), dtype=torch.uint8, device="cuda")
+    rc = lib.moe_nvfp4_quantize_scaled(P(x.data_ptr()), wq.rows, wq.width, ctypes.c_float(1.5),
+                                       P(pq.data_ptr()), P(sq.data_ptr()), s)
+    assert rc == 0
+    del x
+    outq = torch.empty((wq.rows, wq.width), dtype=torch.bfloat16, device="cuda")
+    dq = DirectCall(lib.moe_nvfp4_dequantize, (P(pq.data_ptr()), P(sq.data_ptr()), wq.rows,
+                                               wq.width, ctypes.c_float(1.5), P(outq.data_ptr()), s))
+    measure("dequantize", [dq], wq.rows * (wq.width // 2 + wq.width // 16 + 2 * wq.width),
+            "moe_nvfp4_dequantize, global scale 1.5, [65536, 3072]")
+    return res
+
+
 def main_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -420,6 +507,14 @@ def main_ours(args):
                 "l2": "flushed before every launch" if cold else "inputs larger than L2",
             }
 
+    extensions = {}
+    if not args.no_extra:
+        extensions = extension_measurements(torch, lib, M, W, stream, min(args.steps, 200),
+                                            min(args.warmup, 20), peak)
+        if "compact_flow" in extensions:
+            extensions["compact_flow"]["vs_fused_time"] = round(
+                extensions["compact_flow"]["launch_us_mean"] / (agg["ms_per_step"] * 1e3), 3)
+
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
         return
@@ -441,6 +536,7 @@ def main_ours(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "workloads": others,
+        "extensions": extensions,
     }
     print(json.dumps(line), flush=True)
 
