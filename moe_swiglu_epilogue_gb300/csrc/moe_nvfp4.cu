@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -75,6 +76,18 @@ __device__ __forceinline__ void load_stream_32B(const void* p, uint64_t pol, uin
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
           "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
         : "l"(p), "l"(pol));
+}
+
+__device__ __forceinline__ void load_stream_16B(const void* p, uint64_t pol, uint32_t* r) {
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "l"(p), "l"(pol));
+}
+
+__device__ __forceinline__ void store_32B(void* p, const uint32_t* r) {
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+                    "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
 }
 
 // Programmatic dependent launch: wait until the preceding grid in the stream
@@ -378,19 +391,19 @@ __device__ __forceinline__ uint32_t nibble_by_definition(float y, float d, uint3
 // 2^-13 (relative) away from every half-step boundary. Returns the code.
 template <bool kIeeeRcp>
 __device__ __forceinline__ uint32_t quantize16_exact(const float* v, uint32_t& lo, uint32_t& hi) {
-    const float amax = abs_max16(v);
-    // (scaled values may overflow to inf, which saturates like the definition)
-    const float q = (kIeeeRcp && isinf(amax)) ? amax : div6(amax);
+    // (scaled values may overflow to inf, which saturates like the
+    // definition: clamped to FLT_MAX, every quotient below still saturates)
+    const float amax = kIeeeRcp ? fminf(abs_max16(v), FLT_MAX) : abs_max16(v);
+    const float q = div6(amax);
     const uint32_t code = e4m3x2_rn_sat(0.0f, q) & 0xFFu;
     const float d = e4m3_value(code);
     const float inv = (code == 0u) ? 0.0f : (kIeeeRcp ? __frcp_rn(d) : rcp_approx(d));
     float hs[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-        const float ax = fabsf(v[i]);
+        const float ax = kIeeeRcp ? fminf(fabsf(v[i]), FLT_MAX) : fabsf(v[i]);
         const float q0 = ax * inv;
-        float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);           // |v| / d, corrected
-        if (kIeeeRcp && isinf(ax)) q1 = ax;
+        const float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);     // |v| / d, corrected
         hs[i] = with_sign_of((q1 + kHalfStepBias) - kHalfStepBias, v[i]);
     }
     lo = e2m1x8(hs);
@@ -631,6 +644,7 @@ struct ExArgs {
     int64_t out_rows;               // rows of packed / sf
     uint16_t* out_bf16;             // compact writer output [rows, I]
     float gate_floor;               // most negative gate the window's bound covers
+    uint32_t mid_tol;               // fp32 ulps a BF16 rounding midpoint must be away
 };
 
 // Fast SwiGLU of one block's 16 outputs.
@@ -659,10 +673,13 @@ __device__ __forceinline__ void fast_swiglu16(const FusedArgs& A, const uint32_t
 }
 
 // BF16 values of the 16 outputs by the definition (RN_bf16 of the fp32
-// SwiGLU) as 8 BF16x2 words, element 2p in the low half of word p: each pair
-// of fast values is rounded at both ends of the window; when the ends agree
-// that is the definition's rounding, otherwise the pair is re-evaluated
-// (all lanes needing pair q together).
+// SwiGLU) as 8 BF16x2 words, element 2p in the low half of word p. A BF16
+// rounding midpoint is the fp32 value whose low 16 bits are 0x8000; the
+// window W keeps the definition's fp32 value within W |y| <= W 2^24 ulps
+// of the fast value y, so when y's low half is more than mid_tol ulps from
+// 0x8000 both round alike (a binade edge is 2^15 ulps from any midpoint).
+// The fast pass returns the mask of elements it cannot decide; those are
+// re-evaluated by resolve_bf16_elements.
 __device__ __forceinline__ bool outside_window_range(float g, float u, float y, float gate_floor) {
     // the window bounds the fast path's relative error for gates >=
     // gate_floor and normal results; a BF16 rounding is scale-free, so any
@@ -671,32 +688,60 @@ __device__ __forceinline__ bool outside_window_range(float g, float u, float y, 
     return g < gate_floor || (nonzero && fabsf(y) < 0x1p-100f);
 }
 
-__device__ __forceinline__ void bf16_of_block(const FusedArgs& A, const uint16_t* blk_in, bool valid,
-                                              const uint32_t* w, float gate_floor, const float* y,
-                                              uint32_t* yb) {
+__device__ __forceinline__ uint32_t near_bf16_midpoint(float y, uint32_t tol) {
+    return (((__float_as_uint(y) + (tol - 0x8000u)) & 0xFFFFu) <= 2u * tol) ? 1u : 0u;
+}
+
+__device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool valid, const uint32_t* w,
+                                                       const float* y, uint32_t* yb) {
     uint32_t amb = 0;
 #pragma unroll
     for (int q = 0; q < 8; q++) {
-        const uint32_t lo_end = bf16x2_rn(y[2 * q + 1] * A.Wm1, y[2 * q] * A.Wm1);
-        const uint32_t hi_end = bf16x2_rn(y[2 * q + 1] * A.Wp1, y[2 * q] * A.Wp1);
-        yb[q] = lo_end;
-        const int grp = (2 * q) >> 3, pw = ((2 * q) & 7) >> 1;
-        const uint32_t gw = w[8 * grp + pw], uw = w[8 * grp + 4 + pw];
-        const bool odd = outside_window_range(bf16_lo(gw), bf16_lo(uw), y[2 * q], gate_floor) ||
-                         outside_window_range(bf16_hi(gw), bf16_hi(uw), y[2 * q + 1], gate_floor);
-        amb |= (lo_end != hi_end || odd ? 1u : 0u) << q;
+        yb[q] = bf16x2_rn(y[2 * q + 1], y[2 * q]);
+        amb |= (near_bf16_midpoint(y[2 * q], X.mid_tol) << (2 * q)) |
+               (near_bf16_midpoint(y[2 * q + 1], X.mid_tol) << (2 * q + 1));
     }
-    if (!valid) amb = 0;
-    if (__any_sync(kFullMask, amb != 0u)) {
+    // block pre-test for the window's range (gates below the floor, results
+    // near underflow); element by element only when it fires
+    const uint32_t gmin2 = bf16x2_min(bf16x2_min(bf16x2_min(w[0], w[1]), bf16x2_min(w[2], w[3])),
+                                      bf16x2_min(bf16x2_min(w[8], w[9]), bf16x2_min(w[10], w[11])));
+    float ymin = fabsf(y[0]);
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const bool mine = (amb >> q) & 1u;
-            if (__any_sync(kFullMask, mine) && mine) {
-                float g0, u0, g1, u1;
-                gate_up_at(blk_in, 2 * q, g0, u0);
-                gate_up_at(blk_in, 2 * q + 1, g1, u1);
-                yb[q] = bf16x2_rn(swiglu_precise(g1, u1, A.L), swiglu_precise(g0, u0, A.L));
-            }
+    for (int i = 1; i < 16; i++) ymin = fminf(ymin, fabsf(y[i]));
+    if (fminf(bf16_lo(gmin2), bf16_hi(gmin2)) < X.gate_floor || ymin < 0x1p-100f) {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int grp = i >> 3, pw = (i & 7) >> 1;
+            const uint32_t gw = w[8 * grp + pw], uw = w[8 * grp + 4 + pw];
+            const float g = (i & 1) ? bf16_hi(gw) : bf16_lo(gw);
+            const float u = (i & 1) ? bf16_hi(uw) : bf16_lo(uw);
+            amb |= (outside_window_range(g, u, y[i], X.gate_floor) ? 1u : 0u) << i;
+        }
+    }
+    return valid ? amb : 0u;
+}
+
+// Re-evaluates the undecided elements of kN / 16 blocks (block k of this
+// lane at blk0 + 32 k, element i as bit 16 k + i of `elems`) by the
+// definition path. The warp works through them together: every lane takes
+// its next element each round, so the rounds are the largest count on one
+// lane.
+template <int kN>
+__device__ __forceinline__ void resolve_bf16_elements(const FusedArgs& A, int64_t blk0, uint32_t elems,
+                                                      uint32_t* yb) {
+    static_assert(kN <= 32, "one bit per element");
+    while (__any_sync(kFullMask, elems != 0u)) {
+        if (elems != 0u) {
+            const int j = __ffs(elems) - 1;
+            elems &= elems - 1u;
+            float g, u;
+            gate_up_at(A.gu + (blk0 + 32 * (j >> 4)) * 32, j & 15, g, u);
+            const uint32_t h = bf16x2_rn(0.0f, swiglu_precise(g, u, A.L));   // low half
+            const uint32_t keep = (j & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            const uint32_t put = (j & 1) ? (h << 16) : h;
+#pragma unroll
+            for (int t = 0; t < kN / 2; t++)
+                if (t == (j >> 1)) yb[t] = (yb[t] & keep) | put;
         }
     }
 }
@@ -801,25 +846,13 @@ swiglu_ex_kernel(const ExArgs X) {
     __shared__ int next_chunk;
     if (threadIdx.x == 0) next_chunk = 0;
     __syncthreads();
+    int seg_cursor = -1;        // lane 0: segment of this warp's previous chunk
     for (;;) {                                              // warp-uniform
         int c = 0;
         if (lane == 0) c = atomicAdd(&next_chunk, 1);
         c = __shfl_sync(kFullMask, c, 0);
         const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
         if (base >= cta_end) break;
-        // padded output: the chunk's first row, its column and its segment
-        int64_t r0 = 0, c0 = 0;
-        int e0 = 0;
-        if (padded) {
-            if (lane == 0) {
-                r0 = base / A.bpr;
-                c0 = base - r0 * A.bpr;
-                e0 = segment_of(A.offsets, A.E, r0);
-            }
-            r0 = __shfl_sync(kFullMask, r0, 0);
-            c0 = __shfl_sync(kFullMask, c0, 0);
-            e0 = __shfl_sync(kFullMask, e0, 0);
-        }
         uint32_t w[kUnroll][16];
 #pragma unroll
         for (int k = 0; k < kUnroll; k++) {
@@ -833,46 +866,100 @@ swiglu_ex_kernel(const ExArgs X) {
                 for (int j = 0; j < 16; j++) w[k][j] = 0u;
             }
         }
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + 32 * k + lane;
-            const bool valid = blk < cta_end;
-            int64_t oblk = blk;
-            bool store = valid;
+        // padded output (while the loads are in flight): the chunk's first
+        // row and column, that row's segment, where it ends and its row
+        // shift. A warp's chunks only move forward, so the segment is found
+        // by stepping on from the previous chunk's, or by bisection.
+        int64_t r0 = 0, c0 = 0, seg_end = 0, shift0 = 0;
+        int e0 = 0;
+        if (padded) {
+            if (lane == 0) {
+                r0 = base / A.bpr;
+                c0 = base - r0 * A.bpr;
+                int e = seg_cursor;
+                for (int t = 0; e >= 0 && t < 4 && e + 1 < A.E &&
+                                r0 >= static_cast<int64_t>(__ldg(A.offsets + e + 1)); t++)
+                    e++;
+                if (e < 0 || (e + 1 < A.E && r0 >= static_cast<int64_t>(__ldg(A.offsets + e + 1))))
+                    e = segment_of(A.offsets, A.E, r0);
+                seg_cursor = e0 = e;
+                seg_end = __ldg(A.offsets + e0 + 1);
+                shift0 = static_cast<int64_t>(__ldg(X.out_offsets + e0)) - __ldg(A.offsets + e0);
+            }
+            r0 = __shfl_sync(kFullMask, r0, 0);
+            c0 = __shfl_sync(kFullMask, c0, 0);
+            e0 = __shfl_sync(kFullMask, e0, 0);
+            seg_end = __shfl_sync(kFullMask, seg_end, 0);
+            shift0 = __shfl_sync(kFullMask, shift0, 0);
+        }
+        // output block of block k: its padded position and whether it is stored
+        auto out_block = [&](int k, int64_t blk, bool valid, int64_t& oblk, bool& store) {
+            oblk = blk;
+            store = valid;
             if (padded && valid) {
                 const int64_t j = c0 + 32 * k + lane;
                 const int64_t row = r0 + (A.bpr >= kChunk ? (j >= A.bpr ? 1 : 0) : j / A.bpr);
-                int e = e0;
-                while (e + 1 < A.E && row >= static_cast<int64_t>(__ldg(A.offsets + e + 1))) e++;
-                const int64_t orow = __ldg(X.out_offsets + e) + (row - __ldg(A.offsets + e));
+                int64_t shift = shift0;
+                if (row >= seg_end) {                       // past the chunk's first segment
+                    int e = e0;
+                    while (e + 1 < A.E && row >= static_cast<int64_t>(__ldg(A.offsets + e + 1))) e++;
+                    shift = static_cast<int64_t>(__ldg(X.out_offsets + e)) - __ldg(A.offsets + e);
+                }
+                const int64_t orow = row + shift;
                 store = orow >= 0 && orow < X.out_rows;
-                oblk = orow * A.bpr + (blk - row * A.bpr);
+                oblk = blk + shift * A.bpr;
             }
-            const uint16_t* blk_in = A.gu + blk * 32;
-            float y[16];
-            fast_swiglu16<kBf16Clamp>(A, w[k], y);
-            if (kMode == kExQuantize) {
+        };
+        if (kMode == kExQuantize) {
+#pragma unroll
+            for (int k = 0; k < kUnroll; k++) {
+                const int64_t blk = base + 32 * k + lane;
+                const bool valid = blk < cta_end;
+                int64_t oblk;
+                bool store;
+                out_block(k, blk, valid, oblk, store);
+                float y[16];
+                fast_swiglu16<kBf16Clamp>(A, w[k], y);
                 uint32_t lo, hi, code;
-                scaled_block(X, blk_in, valid, y, lo, hi, code);
+                scaled_block(X, A.gu + blk * 32, valid, y, lo, hi, code);
                 if (store) {
                     *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
                     A.sf[oblk] = static_cast<uint8_t>(code);
                 }
-            } else {
-                uint32_t yb[8];
-                bf16_of_block(A, blk_in, valid, w[k], X.gate_floor, y, yb);
+            }
+        } else {
+            // BF16 values: fast pass over all blocks, one joint re-evaluation
+            // of the undecided pairs, then store or quantize
+            uint32_t yb[8 * kUnroll];
+            uint32_t elems = 0;
+#pragma unroll
+            for (int k = 0; k < kUnroll; k++) {
+                float y[16];
+                fast_swiglu16<kBf16Clamp>(A, w[k], y);
+                elems |= bf16_fast_of_block(X, base + 32 * k + lane < cta_end, w[k], y, yb + 8 * k)
+                         << (16 * k);
+            }
+            resolve_bf16_elements<16 * kUnroll>(A, base + lane, elems, yb);
+#pragma unroll
+            for (int k = 0; k < kUnroll; k++) {
+                const int64_t blk = base + 32 * k + lane;
+                const bool valid = blk < cta_end;
+                const uint32_t* b = yb + 8 * k;
                 if (kMode == kExCompact) {
-                    if (store) {
+                    if (valid) {
                         uint4* dst = reinterpret_cast<uint4*>(X.out_bf16 + blk * 16);
-                        dst[0] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-                        dst[1] = make_uint4(yb[4], yb[5], yb[6], yb[7]);
+                        dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+                        dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
                     }
                 } else {                                // compat: quantize the BF16 values
+                    int64_t oblk;
+                    bool store;
+                    out_block(k, blk, valid, oblk, store);
                     float v[16];
 #pragma unroll
                     for (int q = 0; q < 8; q++) {
-                        v[2 * q] = __fmul_rn(bf16_lo(yb[q]), X.gs);
-                        v[2 * q + 1] = __fmul_rn(bf16_hi(yb[q]), X.gs);
+                        v[2 * q] = __fmul_rn(bf16_lo(b[q]), X.gs);
+                        v[2 * q + 1] = __fmul_rn(bf16_hi(b[q]), X.gs);
                     }
                     uint32_t lo, hi;
                     const uint32_t code = quantize16_exact<true>(v, lo, hi);
@@ -946,35 +1033,85 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
 // Dequantization: NVFP4 -> BF16, value = e2m1 * e4m3 / gs
 // ---------------------------------------------------------------------------
 
-template <bool kScaled>
+enum DequantDivision { kDivNone = 0, kDivMarkstein = 1, kDivIeee = 2 };
+
+// One 16-element block: 8 packed bytes (p), scale value d -> 16 BF16 values.
+template <int kDiv>
+__device__ __forceinline__ void dequantize_block(uint2 p, float d, float gs, float inv_gs,
+                                                 uint16_t* dst16) {
+    uint32_t o[8];
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+        const uint32_t w = half ? p.y : p.x;
+        const uint32_t h2[4] = {e2m1x2_to_f16x2<0>(w), e2m1x2_to_f16x2<1>(w),
+                                e2m1x2_to_f16x2<2>(w), e2m1x2_to_f16x2<3>(w)};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            // e2m1 * e4m3 is exact in fp32 (at most 6 significant bits)
+            float v[2] = {__half2float(__ushort_as_half(static_cast<uint16_t>(h2[k] & 0xFFFFu))) * d,
+                          __half2float(__ushort_as_half(static_cast<uint16_t>(h2[k] >> 16))) * d};
+#pragma unroll
+            for (int t = 0; t < 2; t++) {
+                if (kDiv == kDivMarkstein) {
+                    // Markstein: with inv = RN(1/gs) and q0 = RN(a * inv) within
+                    // one ulp of a/gs, r = a - q0*gs is exact and RN(q0 + r*inv)
+                    // is RN(a/gs) while every quantity stays normal (the host
+                    // takes this path only for such gs). The sign of a zero is
+                    // restored explicitly.
+                    const float q0 = v[t] * inv_gs;
+                    v[t] = copysignf(fmaf(fmaf(-q0, gs, v[t]), inv_gs, q0), v[t]);
+                } else if (kDiv == kDivIeee) {
+                    v[t] = __fdiv_rn(v[t], gs);
+                }
+            }
+            o[4 * half + k] = bf16x2_rn(v[1], v[0]);
+        }
+    }
+    store_32B(dst16, o);
+}
+
+// Lanes take consecutive pairs of blocks, so every load and store of a warp
+// covers whole 32-byte sectors: 16 packed bytes and 2 scale bytes in, two
+// 32-byte stores out. Two pairs per lane are in flight in each iteration; an
+// odd last block is done at the end.
+template <int kDiv>
 __global__ void __launch_bounds__(kThreads)
 nvfp4_dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ sf,
                         int64_t nblk, float gs, uint16_t* __restrict__ out) {
     wait_for_preceding_grid();
     allow_next_grid_launch();
+    const float inv_gs = kDiv == kDivMarkstein ? __frcp_rn(gs) : 1.0f;
+    const uint64_t pol = l2_evict_first_policy();
+    const int64_t npair = nblk / 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t blk = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; blk < nblk;
-         blk += stride) {
-        const uint2 p = *reinterpret_cast<const uint2*>(packed + blk * 8);
-        const float d = e4m3_value(sf[blk]);
-        uint32_t o[8];
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    constexpr int kPairs = 2;
+    for (int64_t p0 = tid; p0 < npair; p0 += kPairs * stride) {
+        uint32_t w[kPairs][4];
+        uint32_t s2[kPairs];
 #pragma unroll
-        for (int half = 0; half < 2; half++) {
-            const uint32_t w = half ? p.y : p.x;
-            const uint32_t h2[4] = {e2m1x2_to_f16x2<0>(w), e2m1x2_to_f16x2<1>(w),
-                                    e2m1x2_to_f16x2<2>(w), e2m1x2_to_f16x2<3>(w)};
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                // e2m1 * e4m3 is exact in fp32 (at most 6 significant bits)
-                float a = __half2float(__ushort_as_half(static_cast<uint16_t>(h2[k] & 0xFFFFu))) * d;
-                float b = __half2float(__ushort_as_half(static_cast<uint16_t>(h2[k] >> 16))) * d;
-                if (kScaled) { a = __fdiv_rn(a, gs); b = __fdiv_rn(b, gs); }
-                o[4 * half + k] = bf16x2_rn(b, a);
+        for (int k = 0; k < kPairs; k++) {
+            const int64_t pi = p0 + k * stride;
+            if (pi < npair) {
+                load_stream_16B(packed + pi * 16, pol, w[k]);
+                s2[k] = __ldg(reinterpret_cast<const uint16_t*>(sf + 2 * pi));
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + blk * 16);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int k = 0; k < kPairs; k++) {
+            const int64_t pi = p0 + k * stride;
+            if (pi < npair) {
+                dequantize_block<kDiv>(make_uint2(w[k][0], w[k][1]), e4m3_value(s2[k] & 0xFFu), gs,
+                                       inv_gs, out + pi * 32);
+                dequantize_block<kDiv>(make_uint2(w[k][2], w[k][3]), e4m3_value(s2[k] >> 8), gs,
+                                       inv_gs, out + pi * 32 + 16);
+            }
+        }
+    }
+    if ((nblk & 1) && tid == 0) {
+        const int64_t blk = nblk - 1;
+        dequantize_block<kDiv>(*reinterpret_cast<const uint2*>(packed + blk * 8), e4m3_value(sf[blk]),
+                               gs, inv_gs, out + blk * 16);
     }
 }
 
@@ -988,6 +1125,7 @@ struct DeviceInfo {
     int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};   // [bf16 clamp][plain, counted, values]
     int occ_ex[2][3] = {{0, 0, 0}, {0, 0, 0}};  // [bf16 clamp][ExMode]
     int occ_quant[2] = {0, 0};                  // [scaled]
+    int occ_dequant = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -1025,7 +1163,9 @@ int device_info(DeviceInfo& out) {
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &di.occ_quant[0], nvfp4_quantize_kernel<false>, kThreads, 0) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &di.occ_quant[1], nvfp4_quantize_kernel<true>, kThreads, 0) != cudaSuccess)
+                &di.occ_quant[1], nvfp4_quantize_kernel<true>, kThreads, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &di.occ_dequant, nvfp4_dequantize_kernel<kDivMarkstein>, kThreads, 0) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
         di.ready = true;
     }
@@ -1195,6 +1335,9 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     if (rows == 0) return MOE_NVFP4_OK;
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    // BF16 roundings compare the fast value itself: W |y| <= W 2^24 ulps,
+    // plus one for the threshold and one for a value on it
+    const double mid_tol = std::ceil(W * 16777216.0) + 2.0;
     // the product with gs rounds once on each side of the comparison
     W += 1.5 * 2.0 * std::ldexp(1.0, -24);
     ExArgs X;
@@ -1204,6 +1347,7 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     X.out_rows = out_offsets != nullptr ? out_rows : rows;
     X.out_bf16 = out_bf16;
     X.gate_floor = static_cast<float>(window_gate_floor(L));
+    X.mid_tol = mid_tol > 32767.0 ? 32767u : static_cast<uint32_t>(mid_tol);
     const int64_t nblk = rows * (I / 16);
     if (bf16_bits_of(L) >= 0) launch_ex_kernel<true>(X, mode, nblk, di, stream);
     else launch_ex_kernel<false>(X, mode, nblk, di, stream);
@@ -1340,14 +1484,22 @@ int moe_nvfp4_dequantize(const uint8_t* packed, const uint8_t* sf, int64_t rows,
     int rc = device_info(di);
     if (rc != MOE_NVFP4_OK) return rc;
     const int64_t nblk = rows * (K / 16);
-    int64_t grid = (nblk + kThreads - 1) / kThreads;
-    if (grid > static_cast<int64_t>(di.sms) * 8) grid = static_cast<int64_t>(di.sms) * 8;
+    int64_t grid = (nblk / 4 + kThreads - 1) / kThreads;     // two pairs per thread
+    if (grid < 1) grid = 1;
+    const int64_t cap = static_cast<int64_t>(di.sms) * di.occ_dequant;
+    if (grid > cap) grid = cap;
+    // e2m1 * e4m3 magnitudes lie in [2^-10, 2688]: for gs in [2^-90, 2^90]
+    // every quotient, residual and RN(1/gs) is a normal fp32 number
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (global_scale == 1.0f)
-        launch(nvfp4_dequantize_kernel<false>, static_cast<int>(grid),
-               reinterpret_cast<cudaStream_t>(stream), packed, sf, nblk, global_scale, out);
+        launch(nvfp4_dequantize_kernel<kDivNone>, static_cast<int>(grid), st, packed, sf, nblk,
+               global_scale, out);
+    else if (global_scale >= 0x1p-90f && global_scale <= 0x1p90f)
+        launch(nvfp4_dequantize_kernel<kDivMarkstein>, static_cast<int>(grid), st, packed, sf,
+               nblk, global_scale, out);
     else
-        launch(nvfp4_dequantize_kernel<true>, static_cast<int>(grid),
-               reinterpret_cast<cudaStream_t>(stream), packed, sf, nblk, global_scale, out);
+        launch(nvfp4_dequantize_kernel<kDivIeee>, static_cast<int>(grid), st, packed, sf, nblk,
+               global_scale, out);
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 

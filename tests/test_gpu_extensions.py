@@ -114,6 +114,21 @@ def test_compact_writer_bit_exact():
         assert np.array_equal(bits(out), oracle.swiglu_bf16(w.data, w.clamp_L))
 
 
+def test_compact_writer_and_compat_near_bf16_midpoints():
+    """Every output within 8 fp32 ulps of a BF16 rounding midpoint: the
+    fast pass cannot decide these, so each goes through the definition."""
+    rng = np.random.default_rng(91)
+    blocks, dist = parity.near_bf16_midpoint_blocks(rng, 512, 7.0)
+    assert dist.max() <= 8 and np.count_nonzero(dist <= 1) > 0
+    gu = blocks.reshape(-1, 8 * 32)                       # I = 128
+    out = M.moe_swiglu_bf16(dev(gu), 7.0)
+    assert np.array_equal(bits(out), oracle.swiglu_bf16(gu, 7.0))
+    for gs in (1.0, 1.7):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(gu), 7.0, global_scale=gs, round_to_bf16=True)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(gu, 7.0, global_scale=gs, round_bf16=True)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+
+
 def test_compact_writer_ragged_rows_untouched():
     w = W.ragged_routing(tokens=128, experts=8, topk=4, I=256, pad_rows=13)
     sent = torch.full((w.rows, w.width), 3.0, dtype=torch.bfloat16, device="cuda")
@@ -145,6 +160,28 @@ def test_dequantize_bit_exact_and_round_trip(gs):
     sf = np.concatenate([codes, np.zeros(1, np.uint8)])[:, None]
     out = M.moe_nvfp4_dequantize(torch.from_numpy(packed).cuda(), torch.from_numpy(sf).cuda(), gs)
     assert np.array_equal(bits(out), oracle.dequantize_nvfp4(packed, sf, gs))
+
+
+def test_dequantize_every_pair_over_global_scales():
+    """Every (nibble, scale code) pair under many global scales: the
+    corrected-reciprocal division in [2^-90, 2^90], its edges, and the IEEE
+    division outside; block counts that are not a multiple of four."""
+    rng = np.random.default_rng(11)
+    scales = [2.0 ** -90, 2.0 ** 90, np.nextafter(np.float32(2.0 ** -90), np.float32(0)),
+              np.nextafter(np.float32(2.0 ** 90), np.float32(np.inf)), 2.0 ** -120, 3e37,
+              1e-30, 7.0, 1.0 / 3.0]
+    scales += list(np.exp(rng.uniform(np.log(1e-6), np.log(1e6), 24)))
+    codes = np.arange(0x7f, dtype=np.uint8)
+    nibs = np.arange(16, dtype=np.uint8)
+    for gs in scales:
+        gs = float(np.float32(gs))
+        for extra_rows in (0, 1, 3):
+            rows = codes.size + extra_rows
+            packed = np.tile((nibs[0::2] | (nibs[1::2] << 4))[None, :], (rows, 1))
+            sf = np.concatenate([codes, rng.integers(0, 0x7f, extra_rows).astype(np.uint8)])[:, None]
+            out = M.moe_nvfp4_dequantize(torch.from_numpy(packed).cuda(),
+                                         torch.from_numpy(np.ascontiguousarray(sf)).cuda(), gs)
+            assert np.array_equal(bits(out), oracle.dequantize_nvfp4(packed, sf, gs)), (gs, rows)
 
 
 @pytest.mark.parametrize("name", ["ragged", "prefill"])
