@@ -208,13 +208,6 @@ __device__ __forceinline__ float div6(float a) {
     return fmaf(r, kInv6, q0);
 }
 
-// silu(a) * b in fast fp32; a, b already clamped.
-__device__ __forceinline__ float silu_times_fast(float a, float b) {
-    const float e = ex2_approx(a * kNegLog2e);   // exp(-a)
-    const float r = rcp_approx(1.0f + e);
-    return (a * r) * b;
-}
-
 // The definition's value: the formula in double precision, rounded once.
 __device__ __noinline__ float swiglu_double(float g, float u, float L) {
     const double a = static_cast<double>(fminf(g, L));
@@ -389,22 +382,50 @@ __device__ __forceinline__ uint32_t nibble_by_definition(float y, float d, uint3
 // v; for BF16-valued v any reciprocal within an ulp works, because the
 // corrected quotient is exact at a tie and elsewhere |v| / d sits at least
 // 2^-13 (relative) away from every half-step boundary. Returns the code.
-template <bool kIeeeRcp>
-__device__ __forceinline__ uint32_t quantize16_exact(const float* v, uint32_t& lo, uint32_t& hi) {
-    // (scaled values may overflow to inf, which saturates like the
-    // definition: clamped to FLT_MAX, every quotient below still saturates)
-    const float amax = kIeeeRcp ? fminf(abs_max16(v), FLT_MAX) : abs_max16(v);
+template <bool kIeeeRcp, bool kPacked>
+__device__ __forceinline__ uint32_t quantize16_exact(const float* v_in, uint32_t& lo, uint32_t& hi) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = v_in[i];
+    float amax = abs_max16(v);
+    if (kIeeeRcp && amax > FLT_MAX) {
+        // an infinity (a scaled value past FLT_MAX): clamped to +-FLT_MAX,
+        // the scale and every infinite element saturate as the definition's
+#pragma unroll
+        for (int i = 0; i < 16; i++) v[i] = fminf(fmaxf(v[i], -FLT_MAX), FLT_MAX);
+        amax = FLT_MAX;
+    }
     const float q = div6(amax);
     const uint32_t code = e4m3x2_rn_sat(0.0f, q) & 0xFFu;
     const float d = e4m3_value(code);
     const float inv = (code == 0u) ? 0.0f : (kIeeeRcp ? __frcp_rn(d) : rcp_approx(d));
     float hs[16];
+    if (kPacked) {
+        // signed quotient v / d corrected as above (every step is odd in v,
+        // so its magnitude is the one |v| / d would give), then the signed
+        // half step: the bias is an even number of half steps, so RN(q +
+        // bias) - bias rounds q to half steps with ties to even on both
+        // sides of zero; the sign of a zero half step is taken from v
+        const float2 inv2 = make_float2(inv, inv), nd2 = make_float2(-d, -d);
+        const float2 bias2 = make_float2(kHalfStepBias, kHalfStepBias);
+        const float2 nbias2 = make_float2(-kHalfStepBias, -kHalfStepBias);
 #pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const float ax = kIeeeRcp ? fminf(fabsf(v[i]), FLT_MAX) : fabsf(v[i]);
-        const float q0 = ax * inv;
-        const float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);     // |v| / d, corrected
-        hs[i] = with_sign_of((q1 + kHalfStepBias) - kHalfStepBias, v[i]);
+        for (int p = 0; p < 8; p++) {
+            const float2 vv = make_float2(v[2 * p], v[2 * p + 1]);
+            const float2 q0 = __fmul2_rn(vv, inv2);
+            const float2 q1 = __ffma2_rn(__ffma2_rn(q0, nd2, vv), inv2, q0);
+            const float2 h = __fadd2_rn(__fadd2_rn(q1, bias2), nbias2);
+            hs[2 * p] = copysignf(h.x, v[2 * p]);
+            hs[2 * p + 1] = copysignf(h.y, v[2 * p + 1]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const float ax = fabsf(v[i]);
+            const float q0 = ax * inv;
+            const float q1 = fmaf(fmaf(-q0, d, ax), inv, q0);     // |v| / d, corrected
+            hs[i] = with_sign_of((q1 + kHalfStepBias) - kHalfStepBias, v[i]);
+        }
     }
     lo = e2m1x8(hs);
     hi = e2m1x8(hs + 8);
@@ -429,6 +450,7 @@ struct FusedArgs {
     float W;                   // relative decision window
     float Wp1, Wm1;            // 1 + W, 1 - W
     float near_thr;            // 0.25 (1 - W)
+    float near_fast;           // 0.25 (1 - W) - 7 W, rounded down: the block test
     const int32_t* offsets;    // [E+1] or null
     int E;
     uint8_t* packed;           // [rows, I/2]
@@ -473,6 +495,67 @@ __device__ __forceinline__ uint32_t scale_by_definition(const uint16_t* blk_in, 
     return e4m3x2_rn_sat(0.0f, __fdiv_rn(am, 6.0f)) & 0xFFu;
 }
 
+// silu(a) * b for two elements at once: the multiplies and the add are
+// packed fp32x2 instructions, each lane rounding as the scalar form does.
+__device__ __forceinline__ float2 silu_times_fast2(float2 a, float2 b) {
+    const float2 x = __fmul2_rn(a, make_float2(kNegLog2e, kNegLog2e));      // -a log2 e
+    const float2 den = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)),
+                                  make_float2(1.0f, 1.0f));
+    return __fmul2_rn(__fmul2_rn(a, make_float2(rcp_approx(den.x), rcp_approx(den.y))), b);
+}
+
+// Fast SwiGLU of one block's 16 outputs from its two loaded 32-byte groups
+// ([gate x8, up x8] twice): deinterleave, clamp, silu(g) u.
+template <bool kBf16Clamp>
+__device__ __forceinline__ void fast_swiglu16(const FusedArgs& A, const uint32_t* w, float* y) {
+    const float L = A.L;
+#pragma unroll
+    for (int grp = 0; grp < 2; grp++) {
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            uint32_t gw = w[8 * grp + p], uw = w[8 * grp + 4 + p];
+            float2 g, u;
+            if (kBf16Clamp) {                        // clamp two values per instruction
+                gw = bf16x2_min(gw, A.L2);
+                uw = bf16x2_min(bf16x2_max(uw, A.negL2), A.L2);
+                g = make_float2(bf16_lo(gw), bf16_hi(gw));
+                u = make_float2(bf16_lo(uw), bf16_hi(uw));
+            } else {
+                g = make_float2(fminf(bf16_lo(gw), L), fminf(bf16_hi(gw), L));
+                u = make_float2(fminf(fmaxf(bf16_lo(uw), -L), L), fminf(fmaxf(bf16_hi(uw), -L), L));
+            }
+            const float2 yv = silu_times_fast2(g, u);
+            y[8 * grp + 2 * p] = yv.x;
+            y[8 * grp + 2 * p + 1] = yv.y;
+        }
+    }
+}
+
+// Half steps of t = y * inv for 16 values, two per packed instruction: hs
+// (signed, ready for the E2M1 cast) and the largest |t - h|. RN(t + bias) -
+// bias rounds t to half steps with ties to even on both sides of zero (the
+// bias 1.5 * 2^22 is an even number of half steps and the spacing there is
+// one half step); it is formed as -h = RN(-t - bias) + bias, which rounds
+// identically, so that t - h is one fma. The sign of a zero half step is
+// taken from y.
+__device__ __forceinline__ float half_steps16(const float* y, float inv, float* hs) {
+    const float2 inv2 = make_float2(inv, inv), ninv2 = make_float2(-inv, -inv);
+    const float2 bias2 = make_float2(kHalfStepBias, kHalfStepBias);
+    const float2 nbias2 = make_float2(-kHalfStepBias, -kHalfStepBias);
+    float r[16];
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const float2 yv = make_float2(y[2 * p], y[2 * p + 1]);
+        const float2 nh = __fadd2_rn(__ffma2_rn(yv, ninv2, nbias2), bias2);
+        const float2 rv = __ffma2_rn(yv, inv2, nh);
+        hs[2 * p] = copysignf(nh.x, y[2 * p]);
+        hs[2 * p + 1] = copysignf(nh.y, y[2 * p + 1]);
+        r[2 * p] = rv.x;
+        r[2 * p + 1] = rv.y;
+    }
+    return abs_max16(r);
+}
+
 // Every lane of the warp calls this together (uniform control flow), with
 // `valid` false for lanes past the end of the stream.
 template <bool kCount, bool kValues, bool kBf16Clamp>
@@ -480,25 +563,7 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
                                             const uint32_t* w, Tally& tally) {
     const float L = A.L;
     float y[16];
-#pragma unroll
-    for (int grp = 0; grp < 2; grp++) {
-#pragma unroll
-        for (int p = 0; p < 4; p++) {
-            uint32_t gw = w[8 * grp + p], uw = w[8 * grp + 4 + p];
-            float g0, g1, u0, u1;
-            if (kBf16Clamp) {                        // clamp two values per instruction
-                gw = bf16x2_min(gw, A.L2);
-                uw = bf16x2_min(bf16x2_max(uw, A.negL2), A.L2);
-                g0 = bf16_lo(gw); g1 = bf16_hi(gw);
-                u0 = bf16_lo(uw); u1 = bf16_hi(uw);
-            } else {
-                g0 = fminf(bf16_lo(gw), L); g1 = fminf(bf16_hi(gw), L);
-                u0 = fminf(fmaxf(bf16_lo(uw), -L), L); u1 = fminf(fmaxf(bf16_hi(uw), -L), L);
-            }
-            y[8 * grp + 2 * p] = silu_times_fast(g0, u0);
-            y[8 * grp + 2 * p + 1] = silu_times_fast(g1, u1);
-        }
-    }
+    fast_swiglu16<kBf16Clamp>(A, w, y);
     if (kValues) {
         if (valid) {
             float4* out = reinterpret_cast<float4*>(A.values + blk * 16);
@@ -521,23 +586,17 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
         if (kCount) tally.scales++;
     }
 
-    // nibbles: half step of t = |y| / d by one fma against the bias; the
-    // block's closeness max_i(|t_i - h_i| + W h_i) flags any t within the
-    // window of a half-step boundary
+    // nibbles: half steps of t = y / d. A t whose true value could lie
+    // across a half-step boundary has |t - h| + W h > 0.25 (1 - W); past
+    // the last nibble-changing boundary (t = 5.25) nothing matters, so h <= 7
+    // there and max |t - h| > 0.25 (1 - W) - 7 W flags every such block
     const float d = e4m3_value(code);
     const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
-    float hs[16], cl[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const float ay = fabsf(y[i]);
-        const float h = fmaf(ay, inv, kHalfStepBias) - kHalfStepBias;
-        cl[i] = fmaf(A.W, h, fabsf(fmaf(ay, inv, -h)));
-        hs[i] = with_sign_of(h, y[i]);
-    }
-    const float closeness = abs_max16(cl);
+    float hs[16];
+    const float closeness = half_steps16(y, inv, hs);
     uint32_t lo = e2m1x8(hs), hi = e2m1x8(hs + 8);
 
-    const bool near = valid && closeness > A.near_thr;
+    const bool near = valid && closeness > A.near_fast;
     if (__any_sync(kFullMask, near)) {
         uint32_t todo = 0;
         if (near) {
@@ -647,31 +706,6 @@ struct ExArgs {
     uint32_t mid_tol;               // fp32 ulps a BF16 rounding midpoint must be away
 };
 
-// Fast SwiGLU of one block's 16 outputs.
-template <bool kBf16Clamp>
-__device__ __forceinline__ void fast_swiglu16(const FusedArgs& A, const uint32_t* w, float* y) {
-    const float L = A.L;
-#pragma unroll
-    for (int grp = 0; grp < 2; grp++) {
-#pragma unroll
-        for (int p = 0; p < 4; p++) {
-            uint32_t gw = w[8 * grp + p], uw = w[8 * grp + 4 + p];
-            float g0, g1, u0, u1;
-            if (kBf16Clamp) {
-                gw = bf16x2_min(gw, A.L2);
-                uw = bf16x2_min(bf16x2_max(uw, A.negL2), A.L2);
-                g0 = bf16_lo(gw); g1 = bf16_hi(gw);
-                u0 = bf16_lo(uw); u1 = bf16_hi(uw);
-            } else {
-                g0 = fminf(bf16_lo(gw), L); g1 = fminf(bf16_hi(gw), L);
-                u0 = fminf(fmaxf(bf16_lo(uw), -L), L); u1 = fminf(fmaxf(bf16_hi(uw), -L), L);
-            }
-            y[8 * grp + 2 * p] = silu_times_fast(g0, u0);
-            y[8 * grp + 2 * p + 1] = silu_times_fast(g1, u1);
-        }
-    }
-}
-
 // BF16 values of the 16 outputs by the definition (RN_bf16 of the fp32
 // SwiGLU) as 8 BF16x2 words, element 2p in the low half of word p. A BF16
 // rounding midpoint is the fp32 value whose low 16 bits are 0x8000; the
@@ -755,7 +789,11 @@ __device__ __forceinline__ void scaled_block(const ExArgs& X, const uint16_t* bl
     const float L = A.L, gs = X.gs;
     float v[16];
 #pragma unroll
-    for (int i = 0; i < 16; i++) v[i] = y[i] * gs;
+    for (int p = 0; p < 8; p++) {
+        const float2 vv = __fmul2_rn(make_float2(y[2 * p], y[2 * p + 1]), make_float2(gs, gs));
+        v[2 * p] = vv.x;
+        v[2 * p + 1] = vv.y;
+    }
     const float amax = abs_max16(v);
     const float q = amax * kInv6;
     const uint32_t ends = e4m3x2_rn_sat(q * A.Wp1, q * A.Wm1);
@@ -774,18 +812,11 @@ __device__ __forceinline__ void scaled_block(const ExArgs& X, const uint16_t* bl
     }
     const float d = e4m3_value(code);
     const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
-    float hs[16], cl[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const float av = fabsf(v[i]);
-        const float h = fmaf(av, inv, kHalfStepBias) - kHalfStepBias;
-        cl[i] = fmaf(A.W, h, fabsf(fmaf(av, inv, -h)));
-        hs[i] = with_sign_of(h, v[i]);
-    }
-    const float closeness = abs_max16(cl);
+    float hs[16];
+    const float closeness = half_steps16(v, inv, hs);      // flags as in the plain step
     lo = e2m1x8(hs);
     hi = e2m1x8(hs + 8);
-    const bool near = valid && closeness > A.near_thr;
+    const bool near = valid && closeness > A.near_fast;
     if (__any_sync(kFullMask, near)) {
         uint32_t todo = 0;
         if (near) {
@@ -962,7 +993,7 @@ swiglu_ex_kernel(const ExArgs X) {
                         v[2 * q + 1] = __fmul_rn(bf16_hi(b[q]), X.gs);
                     }
                     uint32_t lo, hi;
-                    const uint32_t code = quantize16_exact<true>(v, lo, hi);
+                    const uint32_t code = quantize16_exact<true, true>(v, lo, hi);
                     if (store) {
                         *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
                         A.sf[oblk] = static_cast<uint8_t>(code);
@@ -1022,7 +1053,9 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
                 if (kScaled) v[i] = __fmul_rn(v[i], gs);          // two-level: v = fl(x * gs)
             }
             uint32_t lo, hi;
-            const uint32_t code = quantize16_exact<kScaled>(v, lo, hi);
+            // packed quotient steps pay off only with the scaled values
+            // IEEE reciprocal; the BF16 form keeps fewer registers live
+            const uint32_t code = quantize16_exact<kScaled, kScaled>(v, lo, hi);
             *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(lo, hi);
             sf[blk] = static_cast<uint8_t>(code);
         }
@@ -1301,6 +1334,7 @@ FusedArgs fused_args(const uint16_t* gu, int64_t rows, int64_t I, float L, doubl
     A.Wp1 = static_cast<float>(1.0 + W);
     A.Wm1 = static_cast<float>(1.0 - W);
     A.near_thr = static_cast<float>(0.25 * (1.0 - W));
+    A.near_fast = std::nextafter(static_cast<float>(0.25 * (1.0 - W) - 7.0 * W), 0.0f);
     A.offsets = (E > 0) ? offsets : nullptr; A.E = E;
     A.packed = packed; A.sf = sf;
     A.counters = nullptr; A.values = nullptr;
@@ -1377,6 +1411,7 @@ int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int
     A.Wp1 = static_cast<float>(1.0 + W);
     A.Wm1 = static_cast<float>(1.0 - W);
     A.near_thr = static_cast<float>(0.25 * (1.0 - W));
+    A.near_fast = std::nextafter(static_cast<float>(0.25 * (1.0 - W) - 7.0 * W), 0.0f);
     A.offsets = (E > 0) ? offsets : nullptr; A.E = E;
     A.packed = packed; A.sf = sf;
     A.counters = reinterpret_cast<unsigned long long*>(counters); A.values = values;
