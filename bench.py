@@ -96,7 +96,8 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("moe_swiglu_epilogue_gb300/csrc/moe_nvfp4.cu", "include/moe_nvfp4.h"):
+    for rel in ("moe_swiglu_epilogue_gb300/csrc/moe_nvfp4.cu",
+                "moe_swiglu_epilogue_gb300/csrc/nvfp4_device.cuh", "include/moe_nvfp4.h"):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -205,6 +205,51 @@ MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_counted(const uint16_t *gu, int64_t 
                                       int32_t num_experts, uint8_t *packed, uint8_t *sf,
                                       uint64_t *counters, moe_nvfp4_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The step fused into the MoE L1 GEMM's epilogue (the pages' target:
+ * "2026-05-28 Status", priority 3, fuse the amax and FP4 pack into the
+ * L1 -> L2 path; "NVFP4-1.1 Approach, Part 2", the TMEM -> registers -> FP4
+ * epilogue plan). For every expert segment e, rows [offsets[e], offsets[e+1])
+ * of x are multiplied by that expert's weights:
+ *   gu[r, c] = sum_k x[r, k] * w1[e, c, k]     (fp32 accumulation)
+ * and the epilogue applies the fused step above to gu's fp32 values (no
+ * BF16 rounding of gu): output column c takes gate gu[r, 16*(c/8) + c%8]
+ * and up gu[r, 16*(c/8) + 8 + c%8], y = silu(min(g, L)) * clamp(u, -L, L)
+ * in fast fp32, then the NVFP4 block quantization of y exactly as
+ * moe_nvfp4_quantize defines it (applied to fp32 values).
+ *   x        BF16 [rows, H], row-major, 16-byte aligned; H % 64 == 0
+ *   w1       BF16 [num_experts, 2I, H], row-major, 16-byte aligned: row c of
+ *            expert e holds the weights of gu column c (so the rows come in
+ *            [gate x8, up x8] groups); I % 128 == 0
+ *   expert_offsets, num_experts
+ *            DEVICE int32 [num_experts + 1], non-decreasing, required
+ *            (1 <= num_experts <= 2048; one segment [0, rows) for a dense
+ *            GEMM). Offsets are clamped into [0, rows]; rows outside every
+ *            segment are left untouched in packed / sf.
+ *   packed   uint8 [rows, I/2], sf uint8 [rows, I/16], 16-byte aligned
+ *   status   optional DEVICE int32: the kernel writes a nonzero code there
+ *            if one of its internal waits expired (about a second; a fault
+ *            elsewhere on the device); untouched otherwise. May be NULL.
+ * Uses every SM (one CTA each, ~206 KB of shared memory and all 512 TMEM
+ * columns of the SM), tcgen05 tensor cores and TMA. Allocates nothing.
+ * Returns the codes above; MOE_NVFP4_ELAUNCH also when the driver's
+ * tensor-map encoder is unavailable or rejects the tensors.
+ * ------------------------------------------------------------------------- */
+MOE_NVFP4_API int moe_l1_gemm_swiglu_nvfp4(const uint16_t *x, const uint16_t *w1, int64_t rows,
+                                           int64_t H, int64_t I, float clamp_L,
+                                           const int32_t *expert_offsets, int32_t num_experts,
+                                           uint8_t *packed, uint8_t *sf, int32_t *status,
+                                           moe_nvfp4_stream_t stream);
+
+/* Diagnostic: the same GEMM's fp32 accumulators gu [rows, 2I] (16-byte
+ * aligned) for the rows of the segments, in the same accumulation order as
+ * moe_l1_gemm_swiglu_nvfp4 (the same kernel with the epilogue storing the
+ * accumulators instead). */
+MOE_NVFP4_API int moe_l1_gemm_accumulators(const uint16_t *x, const uint16_t *w1, int64_t rows,
+                                           int64_t H, int64_t I, const int32_t *expert_offsets,
+                                           int32_t num_experts, float *acc, int32_t *status,
+                                           moe_nvfp4_stream_t stream);
+
 /* The relative window the fused kernel uses for a clamp L: a scale or
  * nibble decision whose fast-path input lies within this relative distance
  * of a rounding boundary is redone from the definition's SwiGLU value.

@@ -20,6 +20,7 @@ __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_v
            "moe_swiglu_precise_values", "moe_nvfp4_quantize_scaled",
            "moe_swiglu_nvfp4_quantize_ex", "moe_swiglu_bf16", "moe_nvfp4_dequantize",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
+           "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
 
 _lib = None
@@ -75,6 +76,10 @@ def load_library():
     lib.moe_swiglu_bf16.restype = ctypes.c_int
     lib.moe_nvfp4_dequantize.argtypes = [P, P, I64, I64, F, P, P]
     lib.moe_nvfp4_dequantize.restype = ctypes.c_int
+    lib.moe_l1_gemm_swiglu_nvfp4.argtypes = [P, P, I64, I64, I64, F, P, I32, P, P, P, P]
+    lib.moe_l1_gemm_swiglu_nvfp4.restype = ctypes.c_int
+    lib.moe_l1_gemm_accumulators.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P]
+    lib.moe_l1_gemm_accumulators.restype = ctypes.c_int
     lib.moe_nvfp4_abi_version.argtypes = []
     lib.moe_nvfp4_abi_version.restype = ctypes.c_int
     _lib = lib
@@ -312,3 +317,65 @@ def moe_nvfp4_dequantize(packed, sf, global_scale=1.0, out=None, stream=None):
             float(global_scale), ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
     _check(rc, "moe_nvfp4_dequantize")
     return out
+
+
+# ---------------------------------------------------------------------------
+# The step in the L1 GEMM's epilogue
+# ---------------------------------------------------------------------------
+
+def _gemm_operands(x, w1, expert_offsets):
+    torch = _torch()
+    x = _bf16_bits(x, "x", 64)
+    if not w1.is_cuda or w1.dtype not in (torch.bfloat16, torch.uint16, torch.int16) \
+            or w1.dim() != 3 or not w1.is_contiguous():
+        raise ValueError("w1 must be a contiguous BF16 CUDA tensor [experts, 2I, H]")
+    E, two_i, H = w1.shape
+    if H != x.shape[1]:
+        raise ValueError("w1.shape[2] must equal x.shape[1]")
+    if two_i % 256:
+        raise ValueError("w1.shape[1] (2I) must be a multiple of 256")
+    if expert_offsets is None or expert_offsets.dtype != torch.int32 or not expert_offsets.is_cuda \
+            or tuple(expert_offsets.shape) != (E + 1,):
+        raise ValueError(f"expert_offsets must be an int32 CUDA tensor of shape ({E + 1},)")
+    return x, w1, E, two_i // 2, H
+
+
+def moe_l1_gemm_swiglu_nvfp4(x, w1, clamp_L: float, expert_offsets, packed=None, sf=None, status=None,
+                             stream=None):
+    """The fused L1 GEMM: for every expert segment, gu = x_e @ w1[e]^T in
+    fp32, and straight from the accumulators the clamped SwiGLU of its
+    [gate x8, up x8] groups and its NVFP4 quantization.
+    x BF16 [rows, H]; w1 BF16 [E, 2I, H]; expert_offsets int32 [E+1] (device).
+    Returns (packed uint8 [rows, I/2], sf uint8 [rows, I/16]); `status`, an
+    optional int32 CUDA tensor [1], receives a nonzero code if a wait expired."""
+    x, w1, E, I, H = _gemm_operands(x, w1, expert_offsets)
+    rows = x.shape[0]
+    packed = _out(packed, (rows, I // 2), x.device, "packed")
+    sf = _out(sf, (rows, I // 16), x.device, "sf")
+    with _torch().cuda.device(x.device):
+        rc = load_library().moe_l1_gemm_swiglu_nvfp4(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1.data_ptr()), rows, H, I, float(clamp_L),
+            ctypes.c_void_p(expert_offsets.data_ptr()), E, ctypes.c_void_p(packed.data_ptr()),
+            ctypes.c_void_p(sf.data_ptr()), ctypes.c_void_p(0 if status is None else status.data_ptr()),
+            _stream_ptr(stream))
+    _check(rc, "moe_l1_gemm_swiglu_nvfp4")
+    return packed, sf
+
+
+def moe_l1_gemm_accumulators(x, w1, expert_offsets, acc=None, status=None, stream=None):
+    """Diagnostic: the same GEMM's fp32 accumulators [rows, 2I] (rows of
+    the segments written, others untouched)."""
+    torch = _torch()
+    x, w1, E, I, H = _gemm_operands(x, w1, expert_offsets)
+    rows = x.shape[0]
+    if acc is None:
+        acc = torch.zeros((rows, 2 * I), dtype=torch.float32, device=x.device)
+    elif acc.dtype != torch.float32 or tuple(acc.shape) != (rows, 2 * I) or not acc.is_contiguous():
+        raise ValueError(f"acc must be a contiguous float32 CUDA tensor of shape {(rows, 2 * I)}")
+    with torch.cuda.device(x.device):
+        rc = load_library().moe_l1_gemm_accumulators(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1.data_ptr()), rows, H, I,
+            ctypes.c_void_p(expert_offsets.data_ptr()), E, ctypes.c_void_p(acc.data_ptr()),
+            ctypes.c_void_p(0 if status is None else status.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_l1_gemm_accumulators")
+    return acc

@@ -217,6 +217,53 @@ def edge_structured(rows=16384, I=4096, seed=4, L=7.0, adversarial_frac=0.10) ->
     return Workload("edge", "fused", rows, I, gu, clamp_L=L, meta={"kinds": kinds_out})
 
 
+@dataclass
+class GemmWorkload:
+    """Inputs of the L1 GEMM with the step in its epilogue."""
+    name: str
+    rows: int
+    H: int
+    I: int
+    x: np.ndarray                   # uint16 BF16 bits [rows, H]
+    w1: np.ndarray                  # uint16 BF16 bits [experts, 2I, H]
+    offsets: np.ndarray             # int32 [experts + 1]
+    clamp_L: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def active_rows(self) -> int:
+        return int(self.offsets[-1]) - int(self.offsets[0])
+
+    def active_experts(self) -> int:
+        return int(np.count_nonzero(np.diff(self.offsets.astype(np.int64)) > 0))
+
+    def algorithmic_bytes(self) -> int:
+        """x rows read once, every used expert's weights read once, NVFP4 out."""
+        return (self.active_rows * (2 * self.H + self.I // 2 + self.I // 16)
+                + self.active_experts() * 2 * self.I * self.H * 2)
+
+    def flops(self) -> int:
+        return 2 * self.active_rows * self.H * 2 * self.I
+
+
+def gemm_ragged(tokens=4096, experts=256, topk=8, H=7168, I=2048, seed=6, sigma=1.5, L=7.0,
+                pad_rows=0) -> GemmWorkload:
+    """x ~ N(0, 1) and w1 ~ N(0, sigma^2 / H) in BF16, so the accumulators
+    are ~N(0, sigma^2) like the ragged workload's gate/up values; routing as
+    ragged_routing (top-k distinct experts per token, rows grouped by
+    expert). w1 rows come in [gate x8, up x8] groups only by name: every
+    row is drawn alike."""
+    offsets = routing_offsets(tokens, experts, topk, seed)
+    rows = int(offsets[-1]) + pad_rows
+    x = _chunked(rows, H, seed, 7,
+                 lambda rng, n, _: bf16_bits(rng.standard_normal((n, H), dtype=np.float32)))
+    ws = np.float32(sigma / np.sqrt(H))
+    w1 = _chunked(experts * 2 * I, H, seed, 8,
+                  lambda rng, n, _: bf16_bits(rng.standard_normal((n, H), dtype=np.float32) * ws))
+    return GemmWorkload("gemm_ragged", rows, H, I, x, w1.reshape(experts, 2 * I, H), offsets, L,
+                        meta={"tokens": tokens, "experts": experts, "topk": topk})
+
+
 def make(name: str, **kw) -> Workload:
     """Workload by name, at full size unless sizes are given."""
     table = {

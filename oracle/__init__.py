@@ -76,6 +76,9 @@ def _load():
                                                     ctypes.c_int, _P, _P]),
         "swiglu_bf16": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, ctypes.c_int32, _P]),
         "dequantize_nvfp4": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_float, _P]),
+        "swiglu_clamped_f64": (ctypes.c_float, [ctypes.c_double, ctypes.c_double, ctypes.c_float]),
+        "swiglu_clamped_f64_array": (None, [_P, _P, _I64, ctypes.c_float, _P]),
+        "quantize_nvfp4_f32": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -299,3 +302,100 @@ def dequantize_nvfp4(packed: np.ndarray, sf: np.ndarray, global_scale=1.0) -> np
     if _load().dequantize_nvfp4(_ptr(p), _ptr(s), rows, K, float(np.float32(global_scale)), _ptr(out)):
         raise ValueError("oracle dequantize_nvfp4 rejected its arguments")
     return out
+
+
+# ---- the step in the L1 GEMM's epilogue ("2026-05-28 Status", priority 3) ----
+
+def swiglu_clamped_f64(g: float, u: float, clamp_L: float) -> float:
+    return float(_load().swiglu_clamped_f64(float(g), float(u), float(np.float32(clamp_L))))
+
+
+def swiglu_clamped_f64_array(g, u, clamp_L: float) -> np.ndarray:
+    """Clamped SwiGLU of double inputs, each rounded once to fp32."""
+    g = np.ascontiguousarray(g, dtype=np.float64).ravel()
+    u = np.ascontiguousarray(u, dtype=np.float64).ravel()
+    assert g.shape == u.shape
+    y = np.zeros(g.shape[0], np.float32)
+    _load().swiglu_clamped_f64_array(_ptr(g), _ptr(u), g.shape[0], float(clamp_L), _ptr(y))
+    return y
+
+
+def quantize_nvfp4_f32(y: np.ndarray):
+    """fp32 values [rows, K] -> (packed [rows, K/2], sf [rows, K/16])."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    rows, K = y.shape
+    packed = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    if _load().quantize_nvfp4_f32(_ptr(y), rows, K, _ptr(packed), _ptr(sf)):
+        raise ValueError("oracle quantize_nvfp4_f32 rejected its arguments")
+    return packed, sf
+
+
+def _bf16_as_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def l1_gemm_accumulators(x_bf16, w1_bf16, offsets) -> np.ndarray:
+    """gu [rows, 2I] in float64: for expert e, rows [offsets[e], offsets[e+1])
+    of x times w1[e]^T. The products of BF16 values are exact in double and a
+    library matmul sums them, so each value is within ~2^-40 of sum |x w| of
+    the exact one. Rows outside every segment are NaN."""
+    x = _bf16_as_f64(x_bf16)
+    E, two_i, H = w1_bf16.shape
+    rows = x.shape[0]
+    off = np.clip(np.asarray(offsets, np.int64), 0, rows)
+    acc = np.full((rows, two_i), np.nan)
+    for e in range(E):
+        r0, r1 = int(off[e]), max(int(off[e]), int(off[e + 1]))
+        if r1 > r0:
+            acc[r0:r1] = x[r0:r1] @ _bf16_as_f64(w1_bf16[e]).T
+    return acc
+
+
+def l1_gemm_abs_accumulators(x_bf16, w1_bf16, offsets) -> np.ndarray:
+    """sum_k |x[r, k] w1[e, c, k]| per accumulator (the scale of its rounding)."""
+    x = np.abs(_bf16_as_f64(x_bf16))
+    E, two_i, H = w1_bf16.shape
+    rows = x.shape[0]
+    off = np.clip(np.asarray(offsets, np.int64), 0, rows)
+    out = np.full((rows, two_i), np.nan)
+    for e in range(E):
+        r0, r1 = int(off[e]), max(int(off[e]), int(off[e + 1]))
+        if r1 > r0:
+            out[r0:r1] = x[r0:r1] @ np.abs(_bf16_as_f64(w1_bf16[e])).T
+    return out
+
+
+def gemm_swiglu_values(acc: np.ndarray, clamp_L: float) -> np.ndarray:
+    """Deinterleave gu's [gate x8, up x8] column groups ("NVFP4-1.1 Approach
+    Update") and apply the clamped SwiGLU to the (double) accumulators:
+    output column c takes gate gu[:, 16*(c//8) + c%8], up 8 columns on."""
+    rows, two_i = acc.shape
+    I = two_i // 2
+    c = np.arange(I)
+    gate_col = 16 * (c // 8) + c % 8
+    g = np.ascontiguousarray(acc[:, gate_col])
+    u = np.ascontiguousarray(acc[:, gate_col + 8])
+    return swiglu_clamped_f64_array(g, u, clamp_L).reshape(rows, I)
+
+
+def l1_gemm_swiglu_quantize_nvfp4(x_bf16, w1_bf16, offsets, clamp_L: float, packed=None, sf=None,
+                                  acc=None):
+    """The fused L1 GEMM output: NVFP4 of SwiGLU(gu) for the rows of the
+    segments; other rows of packed / sf are left as given. `acc` (float64
+    [rows, 2I]) replaces the exact accumulators when given."""
+    if acc is None:
+        acc = l1_gemm_accumulators(x_bf16, w1_bf16, offsets)
+    rows, two_i = acc.shape
+    I = two_i // 2
+    packed = np.zeros((rows, I // 2), np.uint8) if packed is None else packed.copy()
+    sf = np.zeros((rows, I // 16), np.uint8) if sf is None else sf.copy()
+    off = np.clip(np.asarray(offsets, np.int64), 0, rows)
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), max(int(off[e]), int(off[e + 1]))
+        if r1 > r0:
+            p, s = quantize_nvfp4_f32(gemm_swiglu_values(acc[r0:r1], clamp_L))
+            packed[r0:r1] = p
+            sf[r0:r1] = s
+    return packed, sf

@@ -417,3 +417,36 @@ EXPORT int dequantize_nvfp4(const uint8_t *packed, const uint8_t *sf, int64_t ro
         }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * The step fused into the L1 GEMM's epilogue ("2026-05-28 Status", priority
+ * 3; "NVFP4-1.1 Approach, Part 2", the TMEM -> registers -> FP4 plan): the
+ * GEMM's accumulators gu are real numbers (the test computes them exactly
+ * enough in double precision with a library matmul); the clamped SwiGLU is
+ * applied to them and rounded once to fp32, and the fp32 values are then
+ * quantized block by block exactly as quantize_nvfp4_block defines.
+ * ------------------------------------------------------------------------- */
+
+/* silu(min(g, L)) * clamp(u, -L, L) of double inputs, rounded once to fp32. */
+EXPORT float swiglu_clamped_f64(double g, double u, float L)
+{
+    double a = fmin(g, (double)L);
+    double b = fmin(fmax(u, -(double)L), (double)L);
+    double y = a / (1.0 + exp(-a)) * b;
+    return (float)y;
+}
+
+EXPORT void swiglu_clamped_f64_array(const double *g, const double *u, int64_t n, float L, float *y)
+{
+    for (int64_t i = 0; i < n; i++) y[i] = swiglu_clamped_f64(g[i], u[i], L);
+}
+
+/* fp32 values y [rows, K] -> packed [rows, K/2], sf [rows, K/16]. */
+EXPORT int quantize_nvfp4_f32(const float *y, int64_t rows, int64_t K, uint8_t *packed, uint8_t *sf)
+{
+    if (rows < 0 || K <= 0 || K % 16 != 0) return -1;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t b = 0; b < K / 16; b++)
+            quantize_nvfp4_block(y + r * K + 16 * b, packed + r * (K / 2) + 8 * b, sf + r * (K / 16) + b);
+    return 0;
+}

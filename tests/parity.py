@@ -215,3 +215,47 @@ def near_bf16_midpoint_blocks(rng, n_blocks: int, L: float, max_ulps: int = 8,
     u = np.array(picked_u[:need], np.float32).reshape(n_blocks, 16)
     blocks = W.interleave_gate_up(W.bf16_bits(g), W.bf16_bits(u))
     return blocks, np.array(dist[:need])
+
+
+# ---------------------------------------------------------------------------
+# The L1 GEMM with the step in its epilogue
+# ---------------------------------------------------------------------------
+
+# The epilogue evaluates SwiGLU in fast fp32 on fp32 accumulators; its value
+# is within this relative distance of the oracle's (the fast path's bound on
+# BF16 gates is 1.72e-6; fp32 gates get the same argument rounding, plus
+# margin).
+GEMM_Y_REL_TOL = 4e-6
+GEMM_MAX_MISMATCH_FRACTION = 1e-4
+
+
+def compare_gemm_fused(gpu_packed, gpu_sf, y_ref, rel=GEMM_Y_REL_TOL):
+    """Kernel outputs vs the oracle's fp32 SwiGLU values y_ref [n, I] of the
+    same accumulators. A scale code may differ only where amax * (1 +- rel)
+    / 6 round to different codes; a nibble only where y * (1 +- rel) under
+    the kernel's scale quantizes to the kernel's nibble. Returns (sf
+    mismatches, nibble mismatches, elements); raises on any outside that."""
+    y_ref = np.ascontiguousarray(y_ref, np.float32)
+    n, I = y_ref.shape
+    ref_p, ref_s = oracle.quantize_nvfp4_f32(y_ref)
+    gpu_sf = np.asarray(gpu_sf)
+    amax = np.abs(y_ref.astype(np.float64)).reshape(n, I // 16, 16).max(-1)
+    lo = oracle.fp8_e4m3_from_float32_array((amax * (1 - rel) / 6).astype(np.float32)).reshape(n, -1)
+    hi = oracle.fp8_e4m3_from_float32_array((amax * (1 + rel) / 6).astype(np.float32)).reshape(n, -1)
+    sf_bad = np.argwhere(gpu_sf != ref_s)
+    for r, b in sf_bad:
+        assert lo[r, b] != hi[r, b] and gpu_sf[r, b] in (lo[r, b], hi[r, b]), \
+            ("scale outside tolerance", r, b, gpu_sf[r, b], ref_s[r, b], amax[r, b])
+    gn = unpack_nibbles(gpu_packed)
+    rn = unpack_nibbles(ref_p)
+    bad = np.argwhere(gn != rn)
+    for r, c in bad:
+        code = int(gpu_sf[r, c // 16])
+        y = float(y_ref[r, c])
+        allowed = {oracle.quantize_element_with_scale(v, code)
+                   for v in (y, np.float32(y * (1 - rel)), np.float32(y * (1 + rel)))}
+        assert int(gn[r, c]) in allowed, ("nibble outside tolerance", r, c, y, code, gn[r, c], rn[r, c])
+    nib_mismatch_in_matching_blocks = sum(1 for r, c in bad if gpu_sf[r, c // 16] == ref_s[r, c // 16])
+    assert nib_mismatch_in_matching_blocks <= GEMM_MAX_MISMATCH_FRACTION * gn.size, \
+        (nib_mismatch_in_matching_blocks, gn.size)
+    return len(sf_bad), len(bad), gn.size

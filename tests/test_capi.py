@@ -45,7 +45,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.moe_nvfp4_abi_version() == 2
+    assert lib.moe_nvfp4_abi_version() == 3
     for code in range(0, -9, -1):
         assert lib.moe_nvfp4_strerror(code)
     assert b"unknown" in lib.moe_nvfp4_strerror(-99)

@@ -1,0 +1,143 @@
+"""GPU parity of the L1 GEMM with the step in its epilogue, through the C
+ABI: (1) the kernel's fp32 accumulators against the float64 GEMM within the
+bound of fp32 accumulation; (2) its NVFP4 outputs against the oracle applied
+to those same accumulators, within the fast SwiGLU's tolerance; (3) against
+the oracle on exact accumulators, statistically; rows outside the segments
+untouched; the kernel's wait status stays zero."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_swiglu_epilogue_gb300 as M
+from moe_swiglu_epilogue_gb300 import workloads as W
+
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _ready():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from moe_swiglu_epilogue_gb300 import build
+    build.build()
+    oracle.build()
+    M.load_library()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def acc_bound(H):
+    """fp32 accumulation: one rounding per K-16 MMA step at most, each within
+    2^-24 of the running sum, which is at most sum |x w|; x2 margin."""
+    return (H / 16 + 2) * 2.0 ** -23
+
+
+CASES = {
+    "tiny": dict(tokens=96, experts=4, topk=2, H=256, I=128, seed=31),
+    "ragged_pad": dict(tokens=512, experts=8, topk=2, H=512, I=256, pad_rows=37, seed=32),
+    "dense": dict(tokens=200, experts=1, topk=1, H=1024, I=512, seed=33),
+}
+
+
+def _case(name):
+    return W.gemm_ragged(**CASES[name])
+
+
+def _run(w, acc_too=True):
+    x, w1, off = dev(w.x), dev(w.w1), torch.from_numpy(w.offsets).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows = w.rows
+    sent_p = torch.full((rows, w.I // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    sent_s = torch.full((rows, w.I // 16), 0x5A, dtype=torch.uint8, device="cuda")
+    p, s = M.moe_l1_gemm_swiglu_nvfp4(x, w1, w.clamp_L, off, sent_p, sent_s, status)
+    acc = None
+    if acc_too:
+        acc = M.moe_l1_gemm_accumulators(x, w1, off, status=status)
+    assert int(host(status)[0]) == 0
+    return host(p), host(s), None if acc is None else host(acc)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_accumulators_within_fp32_accumulation_bound(name):
+    w = _case(name)
+    _, _, acc = _run(w)
+    ref = oracle.l1_gemm_accumulators(w.x, w.w1, w.offsets)
+    mag = oracle.l1_gemm_abs_accumulators(w.x, w.w1, w.offsets)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    err = np.abs(acc[r0:r1].astype(np.float64) - ref[r0:r1])
+    assert np.all(err <= acc_bound(w.H) * mag[r0:r1] + 1e-30), (err / mag[r0:r1]).max()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fused_output_matches_the_oracle_on_the_kernels_accumulators(name):
+    w = _case(name)
+    p, s, acc = _run(w)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    y_ref = oracle.gemm_swiglu_values(acc[r0:r1].astype(np.float64), w.clamp_L)
+    sf_bad, nib_bad, n = parity.compare_gemm_fused(p[r0:r1], s[r0:r1], y_ref)
+    assert sf_bad <= 2 and nib_bad <= max(2, n * 1e-4)
+    # rows past the last segment were never written
+    assert np.all(p[r1:] == 0xA5) and np.all(s[r1:] == 0x5A)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fused_output_against_exact_accumulators(name):
+    """The GEMM end to end: nearly every decision equals the oracle's on the
+    exact (float64) accumulators; the rest sit next to a rounding boundary."""
+    w = _case(name)
+    p, s, _ = _run(w, acc_too=False)
+    rp, rs = oracle.l1_gemm_swiglu_quantize_nvfp4(w.x, w.w1, w.offsets, w.clamp_L)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    assert np.mean(s[r0:r1] == rs[r0:r1]) >= 0.999
+    gn, rn = parity.unpack_nibbles(p[r0:r1]), parity.unpack_nibbles(rp[r0:r1])
+    assert np.mean(gn == rn) >= 0.999
+    assert np.all(np.abs(parity.signed_index(gn) - parity.signed_index(rn)) <= 1)
+
+
+def test_segments_with_gaps_and_empty_experts():
+    rng = np.random.default_rng(5)
+    rows, H, I, E = 300, 256, 256, 5
+    x = W.bf16_bits(rng.standard_normal((rows, H)).astype(np.float32))
+    w1 = W.bf16_bits((rng.standard_normal((E, 2 * I, H)) / 10).astype(np.float32))
+    offsets = np.array([7, 7, 140, 141, 141, 290], np.int32)       # gap, empties, one-row expert
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = torch.full((rows, I // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    ss = torch.full((rows, I // 16), 0x5A, dtype=torch.uint8, device="cuda")
+    p, s = M.moe_l1_gemm_swiglu_nvfp4(dev(x), dev(w1).view(E, 2 * I, H), 7.0,
+                                      torch.from_numpy(offsets).cuda(), sp, ss, status)
+    acc = M.moe_l1_gemm_accumulators(dev(x), dev(w1).view(E, 2 * I, H), torch.from_numpy(offsets).cuda(),
+                                     status=status)
+    p, s, acc = host(p), host(s), host(acc)
+    assert int(host(status)[0]) == 0
+    y_ref = oracle.gemm_swiglu_values(acc[7:290].astype(np.float64), 7.0)
+    parity.compare_gemm_fused(p[7:290], s[7:290], y_ref)
+    assert np.all(p[:7] == 0xA5) and np.all(p[290:] == 0xA5)
+    assert np.all(s[:7] == 0x5A) and np.all(s[290:] == 0x5A)
+    ref = oracle.l1_gemm_accumulators(x, w1, offsets)
+    mag = oracle.l1_gemm_abs_accumulators(x, w1, offsets)
+    assert np.all(np.abs(acc[7:290] - ref[7:290]) <= acc_bound(H) * mag[7:290] + 1e-30)
+
+
+def test_full_width_sampled_rows():
+    """H = 7168, I = 2048 (the sizes the benchmark uses), 4 experts; rows
+    sampled from every expert checked against the oracle."""
+    w = W.gemm_ragged(tokens=256, experts=4, topk=2, H=7168, I=2048, seed=21)
+    p, s, acc = _run(w)
+    rng = np.random.default_rng(3)
+    rows = np.sort(rng.choice(np.arange(int(w.offsets[0]), int(w.offsets[-1])), 24, replace=False))
+    sub_off = np.searchsorted(rows, w.offsets).astype(np.int32)       # segments of the sample
+    ref = oracle.l1_gemm_accumulators(w.x[rows], w.w1, sub_off)
+    mag = oracle.l1_gemm_abs_accumulators(w.x[rows], w.w1, sub_off)
+    assert np.all(np.abs(acc[rows] - ref) <= acc_bound(w.H) * mag + 1e-30)
+    y_ref = oracle.gemm_swiglu_values(acc[rows].astype(np.float64), w.clamp_L)
+    parity.compare_gemm_fused(p[rows], s[rows], y_ref)
