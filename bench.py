@@ -447,6 +447,101 @@ def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, pe
     return res
 
 
+GEMM_CASES = (("l1_gemm_decode", 256, 4096, 10), ("l1_gemm_prefill", 256, 32768, 5))
+
+
+def gemm_measurements(torch, lib, M, W, stream, hbm_peak: float, cases=GEMM_CASES, warmup=3,
+                      unfused=True):
+    """The L1 GEMM with the step in its epilogue (BF16 operands, H = 7168,
+    I = 2048, top-8 of 256 experts) on two row sets sharing one seeded weight
+    tensor: 4096 tokens (32768 rows, ~128 per expert: the weights dominate
+    the bytes, so HBM bounds it) and 32768 tokens (262144 rows, ~1024 per
+    expert: the tensor cores bound it). Beside each, the unfused flow the
+    pages' pipeline used: a cuBLAS batched BF16 GEMM over per-expert padded
+    rows writing gu, then the fused activation kernel on gu."""
+    P = ctypes.c_void_p
+    s = P(stream.cuda_stream)
+    H, I = 7168, 2048
+    tflops_peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            tflops_peak = float(json.load(fh).get("bf16_tflops") or 0) or None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {}
+    w1, w1_experts = None, None
+    for name, E, tokens, steps in cases:
+        if w1_experts != E:
+            w1 = None
+            torch.cuda.empty_cache()
+            w1_np = W.gemm_weights(E, H, I)
+            w1 = torch.from_numpy(w1_np.view(np.int16)).cuda()
+            w1_experts = E
+            del w1_np
+        x_np, offsets = W.gemm_rows(tokens, E, 8, H)
+        x = torch.from_numpy(x_np.view(np.int16)).cuda()
+        off = torch.from_numpy(offsets).cuda()
+        rows = x_np.shape[0]
+        active_rows = int(offsets[-1]) - int(offsets[0])
+        del x_np
+        pk = torch.empty((rows, I // 2), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((rows, I // 16), dtype=torch.uint8, device="cuda")
+        call = DirectCall(lib.moe_l1_gemm_swiglu_nvfp4,
+                          (P(x.data_ptr()), P(w1.data_ptr()), rows, H, I, ctypes.c_float(7.0),
+                           P(off.data_ptr()), ctypes.c_int32(E), P(pk.data_ptr()), P(sc.data_ptr()),
+                           P(status.data_ptr()), s))
+        with torch.cuda.stream(stream):
+            _, per, _, _ = time_steps(torch, [call], steps, warmup, stream)
+        fused_s = statistics.fmean(per)
+        entry = {"rows": rows, "tokens": tokens, "H": H, "I": I, "experts": E}
+        active_experts = int(np.count_nonzero(np.diff(offsets.astype(np.int64)) > 0))
+        nbytes = active_rows * (2 * H + I // 2 + I // 16) + active_experts * 2 * I * H * 2
+        flops = 2 * active_rows * H * 2 * I
+        res[name] = entry
+        entry.update({
+            "launch_us_mean": round(fused_s * 1e6, 1),
+            "gbs": round(nbytes / fused_s / 1e9, 1), "frac_of_hbm_peak": round(nbytes / fused_s / 1e9 / hbm_peak, 4),
+            "tflops": round(flops / fused_s / 1e12, 1),
+            "frac_of_bf16_peak": None if tflops_peak is None else round(flops / fused_s / 1e12 / tflops_peak, 4),
+            "bytes": nbytes, "flops": flops,
+            "bound": "hbm" if nbytes / hbm_peak > flops / 1e3 / (tflops_peak or 1e30) else "tensor",
+            "what": "moe_l1_gemm_swiglu_nvfp4 (BF16 x, w1; NVFP4 out); peaks: measured hbm_gbs, bf16_tflops (burst)",
+        })
+        if not unfused:
+            del x, pk, sc
+            continue
+        # unfused: per-expert padded rows, cuBLAS batched GEMM to BF16 gu, then the activation step
+        cnt = np.diff(offsets.astype(np.int64))
+        mx = int(cnt.max())
+        xp = torch.zeros((E, mx, H), dtype=torch.bfloat16, device="cuda")
+        xb = x.view(torch.bfloat16)
+        for e in range(E):
+            xp[e, :cnt[e]] = xb[int(offsets[e]):int(offsets[e + 1])]
+        gu = torch.empty((E, mx, 2 * I), dtype=torch.bfloat16, device="cuda")
+        w1t = w1.view(torch.bfloat16).view(E, 2 * I, H).transpose(1, 2)
+        gu2 = gu.view(E * mx, 2 * I)
+        pk2 = torch.empty((E * mx, I // 2), dtype=torch.uint8, device="cuda")
+        sc2 = torch.empty((E * mx, I // 16), dtype=torch.uint8, device="cuda")
+
+        class Unfused:
+            def __call__(self):
+                torch.bmm(xp, w1t, out=gu)
+                M.moe_swiglu_nvfp4_quantize(gu2, 7.0, None, pk2, sc2, stream=stream)
+        with torch.cuda.stream(stream):
+            _, per_u, _, _ = time_steps(torch, [Unfused()], steps, 2, stream)
+        unfused_s = statistics.fmean(per_u)
+        torch.cuda.synchronize()
+        entry["unfused_cublas_plus_activation_us"] = round(unfused_s * 1e6, 1)
+        entry["fused_vs_unfused_time"] = round(fused_s / unfused_s, 3)
+        del x, pk, sc, xp, gu, gu2, pk2, sc2
+        torch.cuda.empty_cache()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "a GEMM wait expired"
+    del w1
+    torch.cuda.empty_cache()
+    return res
+
+
 def main_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -512,6 +607,7 @@ def main_ours(args):
     if not args.no_extra:
         extensions = extension_measurements(torch, lib, M, W, stream, min(args.steps, 200),
                                             min(args.warmup, 20), peak)
+        extensions.update(gemm_measurements(torch, lib, M, W, stream, peak))
         if "compact_flow" in extensions:
             extensions["compact_flow"]["vs_fused_time"] = round(
                 extensions["compact_flow"]["launch_us_mean"] / (agg["ms_per_step"] * 1e3), 3)
@@ -600,16 +696,38 @@ def parse(argv=None):
                     choices=["ragged", "fused", "prefill", "edge", "quantize", "prefill_quantize"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--gemm-case", default=None, metavar="EXPERTS:TOKENS",
+                    help="time only the L1 GEMM with the step in its epilogue (top-8 routing, "
+                         "H=7168, I=2048) at this size and print its JSON record")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     return ap.parse_args(argv)
+
+
+def main_gemm_case(args):
+    """--gemm-case: the fused L1 GEMM alone at one size (one JSON record)."""
+    import torch
+    torch.cuda.set_device(0)
+    import moe_swiglu_epilogue_gb300 as M
+    from moe_swiglu_epilogue_gb300 import build, workloads as W
+    build.build()
+    lib = M.load_library()
+    stream = torch.cuda.Stream()
+    peak, _ = measured_peaks()
+    E, tokens = (int(v) for v in args.gemm_case.split(":"))
+    res = gemm_measurements(torch, lib, M, W, stream, peak,
+                            cases=((f"l1_gemm_{E}x{tokens}", E, tokens, args.steps),),
+                            warmup=args.warmup, unfused=False)
+    print(json.dumps(res), flush=True)
 
 
 def main(argv=None):
     args = parse(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.gemm_case is not None and args.impl == "ours":
+        main_gemm_case(args)
+    elif args.impl == "reference":
         main_reference(args)
     else:
         main_ours(args)

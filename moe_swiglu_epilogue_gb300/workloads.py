@@ -246,21 +246,34 @@ class GemmWorkload:
         return 2 * self.active_rows * self.H * 2 * self.I
 
 
-def gemm_ragged(tokens=4096, experts=256, topk=8, H=7168, I=2048, seed=6, sigma=1.5, L=7.0,
-                pad_rows=0) -> GemmWorkload:
-    """x ~ N(0, 1) and w1 ~ N(0, sigma^2 / H) in BF16, so the accumulators
-    are ~N(0, sigma^2) like the ragged workload's gate/up values; routing as
-    ragged_routing (top-k distinct experts per token, rows grouped by
-    expert). w1 rows come in [gate x8, up x8] groups only by name: every
-    row is drawn alike."""
+def gemm_weights(experts=256, H=7168, I=2048, seed=6, sigma=1.5) -> np.ndarray:
+    """w1 [experts, 2I, H] BF16 ~ N(0, sigma^2 / H): the accumulators of x ~
+    N(0, 1) rows are then ~N(0, sigma^2), like the ragged workload's gate/up
+    values. Rows come in [gate x8, up x8] groups only by name: every row is
+    drawn alike."""
+    ws = np.float32(sigma / np.sqrt(H))
+    w1 = _chunked(experts * 2 * I, H, seed, 8,
+                  lambda rng, n, _: bf16_bits(rng.standard_normal((n, H), dtype=np.float32) * ws))
+    return w1.reshape(experts, 2 * I, H)
+
+
+def gemm_rows(tokens=4096, experts=256, topk=8, H=7168, seed=6, pad_rows=0):
+    """(x [rows, H] BF16 ~ N(0, 1), offsets) with routing as ragged_routing."""
     offsets = routing_offsets(tokens, experts, topk, seed)
     rows = int(offsets[-1]) + pad_rows
     x = _chunked(rows, H, seed, 7,
                  lambda rng, n, _: bf16_bits(rng.standard_normal((n, H), dtype=np.float32)))
-    ws = np.float32(sigma / np.sqrt(H))
-    w1 = _chunked(experts * 2 * I, H, seed, 8,
-                  lambda rng, n, _: bf16_bits(rng.standard_normal((n, H), dtype=np.float32) * ws))
-    return GemmWorkload("gemm_ragged", rows, H, I, x, w1.reshape(experts, 2 * I, H), offsets, L,
+    return x, offsets
+
+
+def gemm_ragged(tokens=4096, experts=256, topk=8, H=7168, I=2048, seed=6, sigma=1.5, L=7.0,
+                pad_rows=0, w1=None) -> GemmWorkload:
+    """The L1 GEMM's inputs: gemm_rows and gemm_weights (w1 may be passed
+    in to share it between row sets)."""
+    x, offsets = gemm_rows(tokens, experts, topk, H, seed, pad_rows)
+    if w1 is None:
+        w1 = gemm_weights(experts, H, I, seed, sigma)
+    return GemmWorkload("gemm_ragged", x.shape[0], H, I, x, w1, offsets, L,
                         meta={"tokens": tokens, "experts": experts, "topk": topk})
 
 
