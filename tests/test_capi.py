@@ -120,3 +120,27 @@ def test_extension_argument_errors(lib):
     assert dq(A16, A16, 4, 32, 1.0, A16, S) == -3      # output must be 32-byte aligned
     assert dq(NULL, A16, 4, 32, 1.0, A32, S) == -1
     assert dq(NULL, NULL, 0, 32, 1.0, NULL, S) == 0
+
+
+def test_gemm_argument_errors(lib):
+    g = lib.moe_l1_gemm_swiglu_nvfp4
+    # (x, w1, rows, H, I, clamp_L, offsets, E, packed, sf, status, stream)
+    assert g(A16, A16, -1, 64, 128, 7.0, A16, 1, A16, A16, NULL, S) == -4
+    assert g(A16, A16, 4, 96, 128, 7.0, A16, 1, A16, A16, NULL, S) == -2      # H % 64
+    assert g(A16, A16, 4, 64, 192, 7.0, A16, 1, A16, A16, NULL, S) == -2      # I % 128
+    assert g(A16, A16, 4, 64, 128, 0.0, A16, 1, A16, A16, NULL, S) == -5
+    assert g(A16, A16, 4, 64, 128, float("nan"), A16, 1, A16, A16, NULL, S) == -5
+    assert g(A16, A16, 4, 64, 128, 7.0, NULL, 1, A16, A16, NULL, S) == -6     # offsets required
+    assert g(A16, A16, 4, 64, 128, 7.0, A16, 0, A16, A16, NULL, S) == -6
+    assert g(A16, A16, 4, 64, 128, 7.0, A16, 4096, A16, A16, NULL, S) == -6   # > 2048 experts
+    assert g(A16, A16, 4, 64, 2 ** 30, 7.0, A16, 2, A16, A16, NULL, S) == -4  # E * 2I >= 2^31
+    assert g(NULL, A16, 4, 64, 128, 7.0, A16, 1, A16, A16, NULL, S) == -1
+    assert g(A16, A16, 4, 64, 128, 7.0, A16, 1, NULL, A16, NULL, S) == -1
+    assert g(A2, A16, 4, 64, 128, 7.0, A16, 1, A16, A16, NULL, S) == -3
+    assert g(A16, A16, 4, 64, 128, 7.0, A16, 1, A16, A2, NULL, S) == -3
+    assert g(NULL, NULL, 0, 64, 128, 7.0, A16, 1, NULL, NULL, NULL, S) == 0   # nothing to do
+    a = lib.moe_l1_gemm_accumulators
+    # (x, w1, rows, H, I, offsets, E, acc, status, stream)
+    assert a(A16, A16, 4, 64, 128, A16, 1, NULL, NULL, S) == -1
+    assert a(A16, A16, 4, 64, 128, A16, 1, A2, NULL, S) == -3
+    assert a(A16, A16, 4, 100, 128, A16, 1, A16, NULL, S) == -2
