@@ -452,7 +452,16 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
 // A separate kernel, so the plain step above keeps its code as measured.
 // ---------------------------------------------------------------------------
 
-enum ExMode : int { kExQuantize = 0, kExCompat = 1, kExCompact = 2 };
+// kExCompatUnit: the compat mode with global scale 1, where the values to
+// quantize are the BF16 numbers themselves
+enum ExMode : int { kExQuantize = 0, kExCompat = 1, kExCompact = 2, kExCompatUnit = 3 };
+
+// Fast silu's relative error against the definition's fp32 value, in units
+// of 2^-24, at most kSiluErrUlps0 + kSiluErrUlpsPerGate * max(-a, 0) for
+// every BF16 gate a >= -16 (measured exhaustively by the test suite: 3.0
+// for positive gates at any size, up to 13.7 at a = -16).
+constexpr float kSiluErrUlps0 = 4.5f;
+constexpr float kSiluErrUlpsPerGate = 0.8f;
 
 struct ExArgs {
     FusedArgs f;                    // f.W and its derived fields include the global-scale product
@@ -462,6 +471,7 @@ struct ExArgs {
     uint16_t* out_bf16;             // compact writer output [rows, I]
     float gate_floor;               // most negative gate the window's bound covers
     uint32_t mid_tol;               // fp32 ulps a BF16 rounding midpoint must be away
+    int mid_tol_per_block;          // 1: derive it per block from the most negative gate
 };
 
 // BF16 values of the 16 outputs by the definition (RN_bf16 of the fp32
@@ -486,21 +496,32 @@ __device__ __forceinline__ uint32_t near_bf16_midpoint(float y, uint32_t tol) {
 
 __device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool valid, const uint32_t* w,
                                                        const float* y, uint32_t* yb) {
+    const uint32_t gmin2 = bf16x2_min(bf16x2_min(bf16x2_min(w[0], w[1]), bf16x2_min(w[2], w[3])),
+                                      bf16x2_min(bf16x2_min(w[8], w[9]), bf16x2_min(w[10], w[11])));
+    const float gmin = fminf(bf16_lo(gmin2), bf16_hi(gmin2));
+    // the tolerance for this block: 1.5 x (the silu bound at its most
+    // negative gate + 2 for the product and the definition's rounding),
+    // plus one for the threshold and one for a value on it; blocks with a
+    // gate below -16 keep the clamp's global tolerance
+    uint32_t tol = X.mid_tol;
+    if (X.mid_tol_per_block && gmin >= -16.0f) {
+        const float e = fmaf(kSiluErrUlpsPerGate, fmaxf(-gmin, 0.0f), kSiluErrUlps0 + 2.0f);
+        const uint32_t t = static_cast<uint32_t>(ceilf(1.5f * e)) + 2u;
+        tol = t < tol ? t : tol;
+    }
     uint32_t amb = 0;
 #pragma unroll
     for (int q = 0; q < 8; q++) {
         yb[q] = bf16x2_rn(y[2 * q + 1], y[2 * q]);
-        amb |= (near_bf16_midpoint(y[2 * q], X.mid_tol) << (2 * q)) |
-               (near_bf16_midpoint(y[2 * q + 1], X.mid_tol) << (2 * q + 1));
+        amb |= (near_bf16_midpoint(y[2 * q], tol) << (2 * q)) |
+               (near_bf16_midpoint(y[2 * q + 1], tol) << (2 * q + 1));
     }
     // block pre-test for the window's range (gates below the floor, results
     // near underflow); element by element only when it fires
-    const uint32_t gmin2 = bf16x2_min(bf16x2_min(bf16x2_min(w[0], w[1]), bf16x2_min(w[2], w[3])),
-                                      bf16x2_min(bf16x2_min(w[8], w[9]), bf16x2_min(w[10], w[11])));
     float ymin = fabsf(y[0]);
 #pragma unroll
     for (int i = 1; i < 16; i++) ymin = fminf(ymin, fabsf(y[i]));
-    if (fminf(bf16_lo(gmin2), bf16_hi(gmin2)) < X.gate_floor || ymin < 0x1p-100f) {
+    if (gmin < X.gate_floor || ymin < 0x1p-100f) {
 #pragma unroll
         for (int i = 0; i < 16; i++) {
             const int grp = i >> 3, pw = (i & 7) >> 1;
@@ -745,13 +766,22 @@ swiglu_ex_kernel(const ExArgs X) {
                     bool store;
                     out_block(k, blk, valid, oblk, store);
                     float v[16];
+                    uint32_t lo, hi, code;
+                    if (kMode == kExCompatUnit) {               // BF16 values: the cheap exact form
 #pragma unroll
-                    for (int q = 0; q < 8; q++) {
-                        v[2 * q] = __fmul_rn(bf16_lo(b[q]), X.gs);
-                        v[2 * q + 1] = __fmul_rn(bf16_hi(b[q]), X.gs);
+                        for (int q = 0; q < 8; q++) {
+                            v[2 * q] = bf16_lo(b[q]);
+                            v[2 * q + 1] = bf16_hi(b[q]);
+                        }
+                        code = quantize16_exact<false, false>(v, lo, hi);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            v[2 * q] = __fmul_rn(bf16_lo(b[q]), X.gs);
+                            v[2 * q + 1] = __fmul_rn(bf16_hi(b[q]), X.gs);
+                        }
+                        code = quantize16_exact<true, true>(v, lo, hi);
                     }
-                    uint32_t lo, hi;
-                    const uint32_t code = quantize16_exact<true, true>(v, lo, hi);
                     if (store) {
                         *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
                         A.sf[oblk] = static_cast<uint8_t>(code);
@@ -914,7 +944,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};   // [bf16 clamp][plain, counted, values]
-    int occ_ex[2][3] = {{0, 0, 0}, {0, 0, 0}};  // [bf16 clamp][ExMode]
+    int occ_ex[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // [bf16 clamp][ExMode]
     int occ_quant[2] = {0, 0};                  // [scaled]
     int occ_dequant = 0;
 };
@@ -938,7 +968,9 @@ bool ex_occupancy(int* occ) {
            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                &occ[1], swiglu_ex_kernel<kExCompat, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-               &occ[2], swiglu_ex_kernel<kExCompact, kBf16Clamp>, kThreads, 0) == cudaSuccess;
+               &occ[2], swiglu_ex_kernel<kExCompact, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[3], swiglu_ex_kernel<kExCompatUnit, kBf16Clamp>, kThreads, 0) == cudaSuccess;
 }
 
 int device_info(DeviceInfo& out) {
@@ -1105,6 +1137,8 @@ void launch_ex_kernel(const ExArgs& X, int mode, int64_t nblk, const DeviceInfo&
     const int* occ = di.occ_ex[kBf16Clamp ? 1 : 0];
     if (mode == kExQuantize)
         launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp>, grid_for(nblk, di.sms, occ[0]), stream, X);
+    else if (mode == kExCompat && X.gs == 1.0f)
+        launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp>, grid_for(nblk, di.sms, occ[3]), stream, X);
     else if (mode == kExCompat)
         launch(swiglu_ex_kernel<kExCompat, kBf16Clamp>, grid_for(nblk, di.sms, occ[1]), stream, X);
     else
@@ -1140,6 +1174,8 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     X.out_bf16 = out_bf16;
     X.gate_floor = static_cast<float>(window_gate_floor(L));
     X.mid_tol = mid_tol > 32767.0 ? 32767u : static_cast<uint32_t>(mid_tol);
+    // the per-gate silu bound was measured with gates clamped at 100
+    X.mid_tol_per_block = L <= 100.0f ? 1 : 0;
     const int64_t nblk = rows * (I / 16);
     if (bf16_bits_of(L) >= 0) launch_ex_kernel<true>(X, mode, nblk, di, stream);
     else launch_ex_kernel<false>(X, mode, nblk, di, stream);

@@ -195,17 +195,20 @@ def fused_near_tie_blocks(rng, n_blocks: int, L: float, gate_lo: float = -6.0):
 
 
 def near_bf16_midpoint_blocks(rng, n_blocks: int, L: float, max_ulps: int = 8,
-                              candidates: int = 1 << 22):
+                              candidates: int = 1 << 22, gate_range=None):
     """Interleaved BF16 blocks [n, 32] whose oracle fp32 SwiGLU values lie
     within `max_ulps` fp32 ulps of a BF16 rounding midpoint (low 16 bits
     0x8000), where a fast evaluation may round to the other BF16
     neighbour. Drawn by searching random (gate, up) pairs with the oracle;
-    gates ~ N(0, 3^2), ups ~ N(0, 1). Returns (blocks, the distances in
-    ulps)."""
+    gates ~ N(0, 3^2) (or uniform in gate_range), ups ~ N(0, 1). Returns
+    (blocks, the distances in ulps)."""
     picked_g, picked_u, dist = [], [], []
     need = 16 * n_blocks
     while len(picked_g) < need:
-        g = W.bf16_to_f32(W.bf16_bits(rng.standard_normal(candidates, dtype=np.float32) * 3))
+        if gate_range is None:
+            g = W.bf16_to_f32(W.bf16_bits(rng.standard_normal(candidates, dtype=np.float32) * 3))
+        else:
+            g = W.bf16_to_f32(W.bf16_bits(rng.uniform(*gate_range, candidates).astype(np.float32)))
         u = W.bf16_to_f32(W.bf16_bits(rng.standard_normal(candidates, dtype=np.float32)))
         y = oracle.swiglu_clamped_array(g, u, L).astype(np.float32)
         d = np.abs((y.view(np.uint32) & 0xFFFF).astype(np.int64) - 0x8000)

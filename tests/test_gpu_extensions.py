@@ -129,6 +129,46 @@ def test_compact_writer_and_compat_near_bf16_midpoints():
         assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
 
 
+def test_compact_writer_and_compat_near_bf16_midpoints_negative_gates():
+    """The per-block tolerance grows with the most negative gate; here every
+    gate is in [-16, -4] and every output sits next to a BF16 midpoint."""
+    rng = np.random.default_rng(92)
+    blocks, dist = parity.near_bf16_midpoint_blocks(rng, 256, 7.0, gate_range=(-16.0, -4.0))
+    gu = blocks.reshape(-1, 8 * 32)
+    out = M.moe_swiglu_bf16(dev(gu), 7.0)
+    assert np.array_equal(bits(out), oracle.swiglu_bf16(gu, 7.0))
+    for gs in (1.0, 0.6):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(gu), 7.0, global_scale=gs, round_to_bf16=True)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(gu, 7.0, global_scale=gs, round_bf16=True)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
+
+
+def test_per_gate_silu_bound_holds_for_every_bf16_gate():
+    """The BF16 decisions' per-block tolerance rests on the fast silu's
+    relative error being at most c0 + c1 max(-a, 0) units of 2^-24 for every
+    BF16 gate a >= -16 (c0, c1 read from the kernel source). Measured
+    exhaustively with up = 1 (an exact product) and L = 100."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "moe_swiglu_epilogue_gb300", "csrc", "moe_nvfp4.cu")).read()
+    c0 = float(re.search(r"constexpr float kSiluErrUlps0 = ([0-9.]+)f;", src).group(1))
+    c1 = float(re.search(r"constexpr float kSiluErrUlpsPerGate = ([0-9.]+)f;", src).group(1))
+    allg = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    gv = W.bf16_to_f32(allg)
+    gates = allg[np.isfinite(gv) & (gv >= -16.0)]
+    n = gates.size - gates.size % 16
+    up = W.bf16_bits(np.ones(n, np.float32))
+    gu = W.interleave_gate_up(gates[:n].reshape(-1, 16), up.reshape(-1, 16))
+    y_fast = M.moe_swiglu_fast_values(dev(gu), 100.0).cpu().numpy().ravel().astype(np.float64)
+    y_ref = oracle.swiglu_values(gu, 100.0).ravel().astype(np.float64)
+    a = W.bf16_to_f32(gates[:n]).astype(np.float64)
+    nz = y_ref != 0
+    rel = np.abs(y_fast[nz] - y_ref[nz]) / np.abs(y_ref[nz]) / 2.0 ** -24
+    bound = c0 + c1 * np.maximum(-a[nz], 0.0)
+    assert np.all(rel <= bound), float((rel - bound).max())
+
+
 def test_compact_writer_ragged_rows_untouched():
     w = W.ragged_routing(tokens=128, experts=8, topk=4, I=256, pad_rows=13)
     sent = torch.full((w.rows, w.width), 3.0, dtype=torch.bfloat16, device="cuda")
