@@ -510,6 +510,38 @@ def gemm_measurements(torch, lib, M, W, stream, hbm_peak: float, cases=GEMM_CASE
         if not unfused:
             del x, pk, sc
             continue
+        # the pages' two unfused flows with this GEMM: gu (2I BF16) then the
+        # fused activation kernel; the compact SwiGLU (I BF16) then quantize-only
+        gu_o = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device="cuda")
+        sw_o = torch.empty((rows, I), dtype=torch.bfloat16, device="cuda")
+        gemm_gu = DirectCall(lib.moe_l1_gemm_bf16,
+                             (P(x.data_ptr()), P(w1.data_ptr()), rows, H, I, ctypes.c_float(7.0),
+                              P(off.data_ptr()), ctypes.c_int32(E), ctypes.c_int32(0), P(gu_o.data_ptr()),
+                              P(status.data_ptr()), s))
+        act = DirectCall(lib.moe_swiglu_nvfp4_quantize,
+                         (P(gu_o.data_ptr()), rows, I, ctypes.c_float(7.0), P(off.data_ptr()),
+                          ctypes.c_int32(E), P(pk.data_ptr()), P(sc.data_ptr()), s))
+        gemm_sw = DirectCall(lib.moe_l1_gemm_bf16,
+                             (P(x.data_ptr()), P(w1.data_ptr()), rows, H, I, ctypes.c_float(7.0),
+                              P(off.data_ptr()), ctypes.c_int32(E), ctypes.c_int32(1), P(sw_o.data_ptr()),
+                              P(status.data_ptr()), s))
+        qnt = DirectCall(lib.moe_nvfp4_quantize,
+                         (P(sw_o.data_ptr()), rows, I, P(pk.data_ptr()), P(sc.data_ptr()), s))
+
+        class Pair:
+            def __init__(self, a, b):
+                self.a, self.b = a, b
+
+            def __call__(self):
+                self.a()
+                self.b()
+        with torch.cuda.stream(stream):
+            _, per_g, _, _ = time_steps(torch, [Pair(gemm_gu, act)], steps, 2, stream)
+            _, per_c, _, _ = time_steps(torch, [Pair(gemm_sw, qnt)], steps, 2, stream)
+        entry["ours_gu_then_activation_us"] = round(statistics.fmean(per_g) * 1e6, 1)
+        entry["ours_compact_then_quantize_us"] = round(statistics.fmean(per_c) * 1e6, 1)
+        del gu_o, sw_o
+        torch.cuda.empty_cache()
         # unfused: per-expert padded rows, cuBLAS batched GEMM to BF16 gu, then the activation step
         cnt = np.diff(offsets.astype(np.int64))
         mx = int(cnt.max())

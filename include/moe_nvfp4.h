@@ -88,6 +88,7 @@ enum {
     MOE_NVFP4_EOFFSETS = -6,    /* num_experts < 0, or offsets NULL with num_experts > 0 */
     MOE_NVFP4_ELAUNCH = -7,     /* the CUDA launch (or a device query) failed */
     MOE_NVFP4_ESCALE = -8,      /* global_scale not finite, or not > 0 */
+    MOE_NVFP4_EMODE = -9,       /* an unknown output selector */
 };
 
 /*
@@ -249,6 +250,22 @@ MOE_NVFP4_API int moe_l1_gemm_accumulators(const uint16_t *x, const uint16_t *w1
                                            int64_t H, int64_t I, const int32_t *expert_offsets,
                                            int32_t num_experts, float *acc, int32_t *status,
                                            moe_nvfp4_stream_t stream);
+
+/* The unfused flows the pages describe, with the same GEMM (for the
+ * comparison with the fused step and for BF16 consumers):
+ *   output = MOE_L1_GEMM_GU:     out = BF16 gu [rows, 2I] (RN of the fp32
+ *                                accumulators, [gate x8, up x8] columns:
+ *                                "NVFP4-1.1 Approach Update", current flow)
+ *   output = MOE_L1_GEMM_SWIGLU: out = BF16 SwiGLU [rows, I] (RN of the
+ *                                epilogue's fp32 SwiGLU values: the planned
+ *                                compact flow); clamp_L is used only here
+ * out is 16-byte aligned; other arguments as moe_l1_gemm_swiglu_nvfp4.
+ * MOE_NVFP4_EMODE for any other output value. */
+enum { MOE_L1_GEMM_GU = 0, MOE_L1_GEMM_SWIGLU = 1 };
+MOE_NVFP4_API int moe_l1_gemm_bf16(const uint16_t *x, const uint16_t *w1, int64_t rows, int64_t H,
+                                   int64_t I, float clamp_L, const int32_t *expert_offsets,
+                                   int32_t num_experts, int32_t output, uint16_t *out, int32_t *status,
+                                   moe_nvfp4_stream_t stream);
 
 /* The relative window the fused kernel uses for a clamp L: a scale or
  * nibble decision whose fast-path input lies within this relative distance

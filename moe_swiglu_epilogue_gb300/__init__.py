@@ -20,7 +20,7 @@ __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_v
            "moe_swiglu_precise_values", "moe_nvfp4_quantize_scaled",
            "moe_swiglu_nvfp4_quantize_ex", "moe_swiglu_bf16", "moe_nvfp4_dequantize",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
-           "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators",
+           "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators", "moe_l1_gemm_bf16",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
 
 _lib = None
@@ -80,6 +80,8 @@ def load_library():
     lib.moe_l1_gemm_swiglu_nvfp4.restype = ctypes.c_int
     lib.moe_l1_gemm_accumulators.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P]
     lib.moe_l1_gemm_accumulators.restype = ctypes.c_int
+    lib.moe_l1_gemm_bf16.argtypes = [P, P, I64, I64, I64, F, P, I32, I32, P, P, P]
+    lib.moe_l1_gemm_bf16.restype = ctypes.c_int
     lib.moe_nvfp4_abi_version.argtypes = []
     lib.moe_nvfp4_abi_version.restype = ctypes.c_int
     _lib = lib
@@ -379,3 +381,28 @@ def moe_l1_gemm_accumulators(x, w1, expert_offsets, acc=None, status=None, strea
             ctypes.c_void_p(0 if status is None else status.data_ptr()), _stream_ptr(stream))
     _check(rc, "moe_l1_gemm_accumulators")
     return acc
+
+
+def moe_l1_gemm_bf16(x, w1, expert_offsets, output: str = "gu", clamp_L: float = 7.0, out=None,
+                     status=None, stream=None):
+    """The same GEMM writing the BF16 tensors of the unfused flows:
+    output="gu" -> gu [rows, 2I] ([gate x8, up x8] columns), output="swiglu"
+    -> the SwiGLU [rows, I] (clamp_L used only there). Rows outside the
+    segments are left untouched."""
+    torch = _torch()
+    x, w1, E, I, H = _gemm_operands(x, w1, expert_offsets)
+    rows = x.shape[0]
+    sel = {"gu": 0, "swiglu": 1}[output]
+    width = 2 * I if sel == 0 else I
+    if out is None:
+        out = torch.zeros((rows, width), dtype=torch.bfloat16, device=x.device)
+    elif out.dtype not in (torch.bfloat16, torch.int16, torch.uint16) or tuple(out.shape) != (rows, width) \
+            or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous BF16 CUDA tensor of shape {(rows, width)}")
+    with torch.cuda.device(x.device):
+        rc = load_library().moe_l1_gemm_bf16(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1.data_ptr()), rows, H, I, float(clamp_L),
+            ctypes.c_void_p(expert_offsets.data_ptr()), E, sel, ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(0 if status is None else status.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_l1_gemm_bf16")
+    return out

@@ -79,8 +79,15 @@ struct GemmArgs {
     uint8_t* packed;           // [rows, I/2]
     uint8_t* sf;               // [rows, I/16]
     float* acc;                // [rows, 2I] (accumulator diagnostic) or null
+    uint16_t* out_bf16;        // BF16 gu [rows, 2I] or SwiGLU [rows, I] outputs
     int32_t* status;           // optional: nonzero after a wait expired
 };
+
+// What the epilogue writes: the NVFP4 activations (the fused step), the
+// fp32 accumulators (diagnostic), or the BF16 tensors of the unfused flows
+// the pages describe: gu itself ([gate x8, up x8] columns, 2I per row) or
+// the compact SwiGLU (I per row).
+enum GemmOut : int { kOutNvfp4 = 0, kOutAcc = 1, kOutGuBf16 = 2, kOutSwigluBf16 = 3 };
 
 struct SharedState {
     uint64_t full[kStages];
@@ -220,10 +227,8 @@ __device__ __forceinline__ TileCoords tile_coords(const GemmArgs& G, const Share
     return c;
 }
 
-// SwiGLU of one output block (16 outputs) from its 32 accumulator columns,
-// then its exact NVFP4 quantization.
-__device__ __forceinline__ uint32_t epilogue_block(const uint32_t* r, float L, uint32_t& lo, uint32_t& hi) {
-    float y[16];
+// SwiGLU of one output block (16 outputs) from its 32 accumulator columns.
+__device__ __forceinline__ void swiglu_block(const uint32_t* r, float L, float* y) {
 #pragma unroll
     for (int half = 0; half < 2; half++) {
 #pragma unroll
@@ -238,10 +243,16 @@ __device__ __forceinline__ uint32_t epilogue_block(const uint32_t* r, float L, u
             y[8 * half + 2 * p + 1] = v.y;
         }
     }
+}
+
+// ... then its exact NVFP4 quantization.
+__device__ __forceinline__ uint32_t epilogue_block(const uint32_t* r, float L, uint32_t& lo, uint32_t& hi) {
+    float y[16];
+    swiglu_block(r, L, y);
     return quantize16_exact<true, true>(y, lo, hi);
 }
 
-template <bool kAccOut>
+template <int kOut>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                       const GemmArgs G) {
@@ -350,7 +361,35 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             const bool valid = row < c.row_end;
             const uint32_t taddr = S.tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) +
                                    static_cast<uint32_t>(b * kBN);
-            if (kAccOut) {
+            if (kOut == kOutGuBf16 || kOut == kOutSwigluBf16) {
+#pragma unroll 1
+                for (int ob = 0; ob < kBN / 32; ob++) {
+                    uint32_t r[32];
+                    tmem_load32(taddr + 32 * ob, r);
+                    if (kOut == kOutGuBf16) {                       // 32 columns of gu
+                        uint32_t h[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++)
+                            h[j] = bf16x2_rn(__uint_as_float(r[2 * j + 1]), __uint_as_float(r[2 * j]));
+                        if (valid) {
+                            uint4* d4 = reinterpret_cast<uint4*>(G.out_bf16 + row * 2 * G.I + kBN * c.nt + 32 * ob);
+#pragma unroll
+                            for (int j = 0; j < 4; j++) d4[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                        }
+                    } else {                                        // 16 SwiGLU outputs
+                        float y[16];
+                        swiglu_block(r, G.L, y);
+                        uint32_t h[8];
+#pragma unroll
+                        for (int j = 0; j < 8; j++) h[j] = bf16x2_rn(y[2 * j + 1], y[2 * j]);
+                        if (valid) {
+                            uint4* d4 = reinterpret_cast<uint4*>(G.out_bf16 + row * G.I + (kBN / 2) * c.nt + 16 * ob);
+                            d4[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                            d4[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                        }
+                    }
+                }
+            } else if (kOut == kOutAcc) {
                 float* dst = G.acc + row * 2 * G.I + static_cast<int64_t>(kBN) * c.nt;
 #pragma unroll 1
                 for (int ob = 0; ob < kBN / 32; ob++) {
@@ -451,9 +490,14 @@ int gemm_device(int& sms) {
     GemmDevice& d = g_gemm_dev[dev];
     if (!d.ready) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaFuncSetAttribute(l1_gemm_swiglu_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(l1_gemm_swiglu_kernel<kOutNvfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kGemmSmem)) != cudaSuccess ||
-            cudaFuncSetAttribute(l1_gemm_swiglu_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(l1_gemm_swiglu_kernel<kOutAcc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemmSmem)) != cudaSuccess ||
+            cudaFuncSetAttribute(l1_gemm_swiglu_kernel<kOutGuBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGemmSmem)) != cudaSuccess ||
+            cudaFuncSetAttribute(l1_gemm_swiglu_kernel<kOutSwigluBf16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kGemmSmem)) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
         d.ready = true;
@@ -465,20 +509,21 @@ int gemm_device(int& sms) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I, float L,
-                const int32_t* offsets, int32_t E, uint8_t* packed, uint8_t* sf, float* acc,
+                const int32_t* offsets, int32_t E, int mode, uint8_t* packed, uint8_t* sf, void* out,
                 int32_t* status, cudaStream_t stream) {
     if (rows < 0 || rows > (int64_t{1} << 31) - 2 * kBM) return MOE_NVFP4_ESIZE;
     if (H <= 0 || H % kBK != 0 || I <= 0 || I % (kBN / 2) != 0) return MOE_NVFP4_EWIDTH;
-    if (acc == nullptr && !(L > 0.0f && L <= 0x1p64f)) return MOE_NVFP4_ECLAMP;
+    const bool uses_L = mode == kOutNvfp4 || mode == kOutSwigluBf16;
+    if (uses_L && !(L > 0.0f && L <= 0x1p64f)) return MOE_NVFP4_ECLAMP;
     if (E < 1 || E > kMaxGemmExperts || offsets == nullptr) return MOE_NVFP4_EOFFSETS;
     if (static_cast<int64_t>(E) * 2 * I > (int64_t{1} << 31) - 1 || H > (int64_t{1} << 31) - 1)
         return MOE_NVFP4_ESIZE;
     if (rows > 0 && 2 * I > INT64_MAX / 4 / rows) return MOE_NVFP4_ESIZE;
     if (rows == 0) return MOE_NVFP4_OK;
     if (x == nullptr || w1 == nullptr) return MOE_NVFP4_ENULL;
-    if (acc == nullptr && (packed == nullptr || sf == nullptr)) return MOE_NVFP4_ENULL;
-    if (!aligned16(x) || !aligned16(w1) || (acc != nullptr && !aligned16(acc)) ||
-        (acc == nullptr && (!aligned16(packed) || !aligned16(sf))))
+    if (mode == kOutNvfp4 ? (packed == nullptr || sf == nullptr) : out == nullptr) return MOE_NVFP4_ENULL;
+    if (!aligned16(x) || !aligned16(w1) ||
+        (mode == kOutNvfp4 ? (!aligned16(packed) || !aligned16(sf)) : !aligned16(out)))
         return MOE_NVFP4_EALIGN;
     int sms = 0;
     int rc = gemm_device(sms);
@@ -488,8 +533,10 @@ int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, 
         return MOE_NVFP4_ELAUNCH;
     GemmArgs G;
     G.offsets = offsets; G.E = E; G.rows = rows; G.H = H; G.I = I;
-    G.nt = static_cast<int>(2 * I / kBN); G.L = L;
-    G.packed = packed; G.sf = sf; G.acc = acc; G.status = status;
+    G.nt = static_cast<int>(2 * I / kBN); G.L = uses_L ? L : 1.0f;
+    G.packed = packed; G.sf = sf; G.status = status;
+    G.acc = mode == kOutAcc ? static_cast<float*>(out) : nullptr;
+    G.out_bf16 = (mode == kOutGuBf16 || mode == kOutSwigluBf16) ? static_cast<uint16_t*>(out) : nullptr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms));
     cfg.blockDim = dim3(kGemmThreads);
@@ -500,8 +547,13 @@ int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = acc != nullptr ? cudaLaunchKernelEx(&cfg, l1_gemm_swiglu_kernel<true>, tmX, tmW, G)
-                                   : cudaLaunchKernelEx(&cfg, l1_gemm_swiglu_kernel<false>, tmX, tmW, G);
+    cudaError_t e;
+    switch (mode) {
+        case kOutNvfp4: e = cudaLaunchKernelEx(&cfg, l1_gemm_swiglu_kernel<kOutNvfp4>, tmX, tmW, G); break;
+        case kOutAcc: e = cudaLaunchKernelEx(&cfg, l1_gemm_swiglu_kernel<kOutAcc>, tmX, tmW, G); break;
+        case kOutGuBf16: e = cudaLaunchKernelEx(&cfg, l1_gemm_swiglu_kernel<kOutGuBf16>, tmX, tmW, G); break;
+        default: e = cudaLaunchKernelEx(&cfg, l1_gemm_swiglu_kernel<kOutSwigluBf16>, tmX, tmW, G); break;
+    }
     return e == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 
@@ -512,15 +564,23 @@ extern "C" {
 int moe_l1_gemm_swiglu_nvfp4(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,
                              float clamp_L, const int32_t* expert_offsets, int32_t num_experts,
                              uint8_t* packed, uint8_t* sf, int32_t* status, moe_nvfp4_stream_t stream) {
-    return launch_gemm(x, w1, rows, H, I, clamp_L, expert_offsets, num_experts, packed, sf, nullptr, status,
-                       reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm(x, w1, rows, H, I, clamp_L, expert_offsets, num_experts, kOutNvfp4, packed, sf,
+                       nullptr, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_l1_gemm_accumulators(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,
                              const int32_t* expert_offsets, int32_t num_experts, float* acc,
                              int32_t* status, moe_nvfp4_stream_t stream) {
-    if (acc == nullptr && rows > 0) return MOE_NVFP4_ENULL;
-    return launch_gemm(x, w1, rows, H, I, 1.0f, expert_offsets, num_experts, nullptr, nullptr, acc, status,
+    return launch_gemm(x, w1, rows, H, I, 1.0f, expert_offsets, num_experts, kOutAcc, nullptr, nullptr, acc,
+                       status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_l1_gemm_bf16(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,
+                     float clamp_L, const int32_t* expert_offsets, int32_t num_experts, int32_t output,
+                     uint16_t* out, int32_t* status, moe_nvfp4_stream_t stream) {
+    if (output != MOE_L1_GEMM_GU && output != MOE_L1_GEMM_SWIGLU) return MOE_NVFP4_EMODE;
+    return launch_gemm(x, w1, rows, H, I, clamp_L, expert_offsets, num_experts,
+                       output == MOE_L1_GEMM_GU ? kOutGuBf16 : kOutSwigluBf16, nullptr, nullptr, out, status,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 

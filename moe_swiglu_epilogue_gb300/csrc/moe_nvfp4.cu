@@ -1345,10 +1345,11 @@ const char* moe_nvfp4_strerror(int code) {
         case MOE_NVFP4_EOFFSETS: return "num_experts < 0, or expert offsets missing";
         case MOE_NVFP4_ELAUNCH: return "CUDA launch or device query failed";
         case MOE_NVFP4_ESCALE: return "global_scale must be finite and > 0";
+        case MOE_NVFP4_EMODE: return "unknown output selector";
         default: return "unknown error code";
     }
 }
 
-int moe_nvfp4_abi_version(void) { return 3; }
+int moe_nvfp4_abi_version(void) { return 4; }
 
 }  // extern "C"

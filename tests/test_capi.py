@@ -45,8 +45,8 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.moe_nvfp4_abi_version() == 3
-    for code in range(0, -9, -1):
+    assert lib.moe_nvfp4_abi_version() == 4
+    for code in range(0, -10, -1):
         assert lib.moe_nvfp4_strerror(code)
     assert b"unknown" in lib.moe_nvfp4_strerror(-99)
 
@@ -144,3 +144,10 @@ def test_gemm_argument_errors(lib):
     assert a(A16, A16, 4, 64, 128, A16, 1, NULL, NULL, S) == -1
     assert a(A16, A16, 4, 64, 128, A16, 1, A2, NULL, S) == -3
     assert a(A16, A16, 4, 100, 128, A16, 1, A16, NULL, S) == -2
+    b = lib.moe_l1_gemm_bf16
+    # (x, w1, rows, H, I, clamp_L, offsets, E, output, out, status, stream)
+    assert b(A16, A16, 4, 64, 128, 7.0, A16, 1, 2, A16, NULL, S) == -9          # unknown output
+    assert b(A16, A16, 4, 64, 128, 0.0, A16, 1, 1, A16, NULL, S) == -5          # SwiGLU needs L
+    assert b(A16, A16, 4, 64, 128, 7.0, A16, 1, 0, NULL, NULL, S) == -1
+    assert b(A16, A16, 4, 64, 128, 7.0, A16, 1, 0, A2, NULL, S) == -3
+    assert b(A16, A16, 0, 64, 128, 0.0, A16, 1, 0, NULL, NULL, S) == 0         # gu ignores L

@@ -141,3 +141,42 @@ def test_full_width_sampled_rows():
     assert np.all(np.abs(acc[rows] - ref) <= acc_bound(w.H) * mag + 1e-30)
     y_ref = oracle.gemm_swiglu_values(acc[rows].astype(np.float64), w.clamp_L)
     parity.compare_gemm_fused(p[rows], s[rows], y_ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_pad"])
+def test_bf16_outputs_of_the_unfused_flows(name):
+    """gu: the RN_bf16 of the kernel's accumulators (bit for bit, same MMA
+    sequence) and within half a BF16 ulp plus the accumulation bound of the
+    exact GEMM. SwiGLU: the oracle's SwiGLU of those accumulators rounded to
+    BF16, except one-ulp differences where that value lies within the fast
+    SwiGLU's tolerance of a BF16 midpoint. Rows outside the segments stay."""
+    w = _case(name)
+    x, w1, off = dev(w.x), dev(w.w1), torch.from_numpy(w.offsets).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows, I = w.rows, w.I
+    sent = 0x4040
+    gu = torch.full((rows, 2 * I), sent, dtype=torch.int16, device="cuda")
+    sw = torch.full((rows, I), sent, dtype=torch.int16, device="cuda")
+    M.moe_l1_gemm_bf16(x, w1, off, "gu", out=gu, status=status)
+    M.moe_l1_gemm_bf16(x, w1, off, "swiglu", w.clamp_L, out=sw, status=status)
+    acc = host(M.moe_l1_gemm_accumulators(x, w1, off, status=status))
+    assert int(host(status)[0]) == 0
+    gu, sw = host(gu).view(np.uint16), host(sw).view(np.uint16)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    assert np.all(gu[:r0] == sent) and np.all(gu[r1:] == sent)
+    assert np.all(sw[:r0] == sent) and np.all(sw[r1:] == sent)
+    assert np.array_equal(gu[r0:r1], W.bf16_bits(acc[r0:r1]))
+    ref = oracle.l1_gemm_accumulators(w.x, w.w1, w.offsets)[r0:r1]
+    mag = oracle.l1_gemm_abs_accumulators(w.x, w.w1, w.offsets)[r0:r1]
+    g = W.bf16_to_f32(gu[r0:r1]).reshape(r1 - r0, 2 * I).astype(np.float64)
+    half_ulp = np.abs(g) * 2.0 ** -8
+    assert np.all(np.abs(g - ref) <= half_ulp + acc_bound(w.H) * mag + 1e-30)
+    y = oracle.gemm_swiglu_values(acc[r0:r1].astype(np.float64), w.clamp_L)
+    want = W.bf16_bits(y)
+    bad = np.argwhere(sw[r0:r1] != want)
+    for r, c in bad:
+        yv = np.float64(y[r, c])
+        lo = W.bf16_bits(np.float32(yv * (1 - parity.GEMM_Y_REL_TOL)))
+        hi = W.bf16_bits(np.float32(yv * (1 + parity.GEMM_Y_REL_TOL)))
+        assert lo != hi and sw[r0 + r, c] in (lo, hi), (r, c, yv)
+    assert bad.shape[0] <= max(2, 1e-4 * want.size)
