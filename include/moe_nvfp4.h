@@ -267,6 +267,20 @@ MOE_NVFP4_API int moe_l1_gemm_bf16(const uint16_t *x, const uint16_t *w1, int64_
                                    int32_t num_experts, int32_t output, uint16_t *out, int32_t *status,
                                    moe_nvfp4_stream_t stream);
 
+/* Diagnostic of the failure path: moe_l1_gemm_swiglu_nvfp4's kernel with
+ * its loads withheld (nothing ever completes the first stage) and every
+ * internal wait limited to wait_cycles SM clock cycles (1000 ..
+ * 2e9). Each role stops when its wait expires or another role's did: the
+ * DEVICE int32 status (required here) receives the code of an expired wait
+ * (1 producer / free stage, 2 MMA issuer / free accumulator, 3 MMA issuer /
+ * loaded stage, 4 epilogue / finished accumulator), the TMEM is released,
+ * and packed / sf are not written. The kernels run normally afterwards. */
+MOE_NVFP4_API int moe_l1_gemm_wait_selftest(const uint16_t *x, const uint16_t *w1, int64_t rows,
+                                            int64_t H, int64_t I, const int32_t *expert_offsets,
+                                            int32_t num_experts, uint8_t *packed, uint8_t *sf,
+                                            int32_t *status, int64_t wait_cycles,
+                                            moe_nvfp4_stream_t stream);
+
 /* The relative window the fused kernel uses for a clamp L: a scale or
  * nibble decision whose fast-path input lies within this relative distance
  * of a rounding boundary is redone from the definition's SwiGLU value.

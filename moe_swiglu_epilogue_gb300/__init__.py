@@ -21,6 +21,7 @@ __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_v
            "moe_swiglu_nvfp4_quantize_ex", "moe_swiglu_bf16", "moe_nvfp4_dequantize",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
            "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators", "moe_l1_gemm_bf16",
+           "moe_l1_gemm_wait_selftest",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
 
 _lib = None
@@ -80,6 +81,8 @@ def load_library():
     lib.moe_l1_gemm_swiglu_nvfp4.restype = ctypes.c_int
     lib.moe_l1_gemm_accumulators.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P]
     lib.moe_l1_gemm_accumulators.restype = ctypes.c_int
+    lib.moe_l1_gemm_wait_selftest.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P, I64, P]
+    lib.moe_l1_gemm_wait_selftest.restype = ctypes.c_int
     lib.moe_l1_gemm_bf16.argtypes = [P, P, I64, I64, I64, F, P, I32, I32, P, P, P]
     lib.moe_l1_gemm_bf16.restype = ctypes.c_int
     lib.moe_nvfp4_abi_version.argtypes = []
@@ -406,3 +409,22 @@ def moe_l1_gemm_bf16(x, w1, expert_offsets, output: str = "gu", clamp_L: float =
             ctypes.c_void_p(0 if status is None else status.data_ptr()), _stream_ptr(stream))
     _check(rc, "moe_l1_gemm_bf16")
     return out
+
+
+def moe_l1_gemm_wait_selftest(x, w1, expert_offsets, status, wait_cycles: int, packed=None, sf=None,
+                              stream=None):
+    """Diagnostic of the failure path: the fused GEMM with its loads
+    withheld and every wait limited to wait_cycles; `status` (int32 CUDA
+    tensor [1]) receives the code of the wait that expired."""
+    x, w1, E, I, H = _gemm_operands(x, w1, expert_offsets)
+    rows = x.shape[0]
+    packed = _out(packed, (rows, I // 2), x.device, "packed")
+    sf = _out(sf, (rows, I // 16), x.device, "sf")
+    with _torch().cuda.device(x.device):
+        rc = load_library().moe_l1_gemm_wait_selftest(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1.data_ptr()), rows, H, I,
+            ctypes.c_void_p(expert_offsets.data_ptr()), E, ctypes.c_void_p(packed.data_ptr()),
+            ctypes.c_void_p(sf.data_ptr()), ctypes.c_void_p(status.data_ptr()), int(wait_cycles),
+            _stream_ptr(stream))
+    _check(rc, "moe_l1_gemm_wait_selftest")
+    return packed, sf

@@ -59,7 +59,7 @@ constexpr uint32_t kStageA = kBM * kBK * 2;
 constexpr uint32_t kStageB = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = 2 * kBN;      // two accumulators
-constexpr long long kWaitCycles = 2000000000LL;
+constexpr long long kWaitCycles = 2000000000LL;   // about a second
 constexpr int kMaxGemmDevices = 64;
 
 // tcgen05 instruction descriptor, kind::f16: fp32 D (bits 4-5 = 1), BF16 A
@@ -81,6 +81,8 @@ struct GemmArgs {
     float* acc;                // [rows, 2I] (accumulator diagnostic) or null
     uint16_t* out_bf16;        // BF16 gu [rows, 2I] or SwiGLU [rows, I] outputs
     int32_t* status;           // optional: nonzero after a wait expired
+    long long wait_cycles;     // limit of every mbarrier wait
+    int withhold_loads;        // diagnostic: the producer issues nothing
 };
 
 // What the epilogue writes: the NVFP4 activations (the fused step), the
@@ -111,15 +113,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of the given parity; false once the CTA aborted or
-// the wait expired (which records `code` and aborts the CTA).
+// the wait expired (which records `code` and aborts the CTA). Codes: 1 the
+// producer waiting for a free stage, 2 the MMA issuer for a free
+// accumulator, 3 the MMA issuer for a loaded stage, 4 the epilogue for a
+// finished accumulator.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, SharedState& S,
-                                          int32_t* status, int code) {
+                                          int32_t* status, int code, long long limit) {
     const long long t0 = clock64();
     for (uint32_t n = 0;; n++) {
         if (mbar_try(bar, parity)) return true;
         if ((n & 31) == 31) {
             if (*reinterpret_cast<volatile int*>(&S.abort)) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 *reinterpret_cast<volatile int*>(&S.abort) = 1;
                 if (status != nullptr) atomicExch(status, code);
                 return false;
@@ -304,7 +309,7 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const int nkb = static_cast<int>(G.H / kBK);
 
     if (warp == 0) {
-        if (lane == 0) {                                            // TMA producer
+        if (lane == 0 && !G.withhold_loads) {                       // TMA producer
             uint32_t it = 0;
             for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
                 const TileCoords c = tile_coords(G, S, t);
@@ -312,7 +317,7 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                 for (int kb = 0; kb < nkb; kb++, it++) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1u, S, G.status, 1)) goto done;
+                    if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1u, S, G.status, 1, G.wait_cycles)) goto done;
                     uint8_t* st = base + s * kStageBytes;
                     mbar_expect_tx(&S.full[s], kStageBytes);
                     tma_load_2d(st, &tmX, kb * kBK, static_cast<int>(c.row0), &S.full[s]);
@@ -326,13 +331,13 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             for (int64_t t = blockIdx.x; t < total; t += gridDim.x, local++) {
                 const int b = static_cast<int>(local & 1u);
                 const uint32_t aph = (local >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&S.acc_empty[b]), aph ^ 1u, S, G.status, 2)) goto done;
+                if (!mbar_wait(smem_u32(&S.acc_empty[b]), aph ^ 1u, S, G.status, 2, G.wait_cycles)) goto done;
                 tmem_fence_after();
                 const uint32_t d_tmem = S.tmem_base + static_cast<uint32_t>(b * kBN);
                 for (int kb = 0; kb < nkb; kb++, it++) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&S.full[s]), ph, S, G.status, 3)) goto done;
+                    if (!mbar_wait(smem_u32(&S.full[s]), ph, S, G.status, 3, G.wait_cycles)) goto done;
                     tmem_fence_after();
                     const uint8_t* st = base + s * kStageBytes;
                     const uint64_t da = sw128_kmajor_desc(st), db = sw128_kmajor_desc(st + kStageA);
@@ -353,7 +358,7 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             const uint32_t aph = (local >> 1) & 1u;
             // tcgen05.ld is warp-collective: the warp goes on only if every
             // lane saw the accumulator complete
-            const bool ok = mbar_wait(smem_u32(&S.acc_full[b]), aph, S, G.status, 4);
+            const bool ok = mbar_wait(smem_u32(&S.acc_full[b]), aph, S, G.status, 4, G.wait_cycles);
             if (!__all_sync(kFullMask, ok)) break;
             tmem_fence_after();
             const TileCoords c = tile_coords(G, S, t);
@@ -510,7 +515,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I, float L,
                 const int32_t* offsets, int32_t E, int mode, uint8_t* packed, uint8_t* sf, void* out,
-                int32_t* status, cudaStream_t stream) {
+                int32_t* status, cudaStream_t stream, long long wait_cycles = kWaitCycles,
+                int withhold_loads = 0) {
     if (rows < 0 || rows > (int64_t{1} << 31) - 2 * kBM) return MOE_NVFP4_ESIZE;
     if (H <= 0 || H % kBK != 0 || I <= 0 || I % (kBN / 2) != 0) return MOE_NVFP4_EWIDTH;
     const bool uses_L = mode == kOutNvfp4 || mode == kOutSwigluBf16;
@@ -535,6 +541,7 @@ int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, 
     G.offsets = offsets; G.E = E; G.rows = rows; G.H = H; G.I = I;
     G.nt = static_cast<int>(2 * I / kBN); G.L = uses_L ? L : 1.0f;
     G.packed = packed; G.sf = sf; G.status = status;
+    G.wait_cycles = wait_cycles; G.withhold_loads = withhold_loads;
     G.acc = mode == kOutAcc ? static_cast<float*>(out) : nullptr;
     G.out_bf16 = (mode == kOutGuBf16 || mode == kOutSwigluBf16) ? static_cast<uint16_t*>(out) : nullptr;
     cudaLaunchConfig_t cfg = {};
@@ -573,6 +580,15 @@ int moe_l1_gemm_accumulators(const uint16_t* x, const uint16_t* w1, int64_t rows
                              int32_t* status, moe_nvfp4_stream_t stream) {
     return launch_gemm(x, w1, rows, H, I, 1.0f, expert_offsets, num_experts, kOutAcc, nullptr, nullptr, acc,
                        status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_l1_gemm_wait_selftest(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,
+                              const int32_t* expert_offsets, int32_t num_experts, uint8_t* packed,
+                              uint8_t* sf, int32_t* status, int64_t wait_cycles, moe_nvfp4_stream_t stream) {
+    if (status == nullptr) return MOE_NVFP4_ENULL;
+    if (wait_cycles < 1000 || wait_cycles > kWaitCycles) return MOE_NVFP4_ESIZE;
+    return launch_gemm(x, w1, rows, H, I, 7.0f, expert_offsets, num_experts, kOutNvfp4, packed, sf, nullptr,
+                       status, reinterpret_cast<cudaStream_t>(stream), wait_cycles, 1);
 }
 
 int moe_l1_gemm_bf16(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,

@@ -151,3 +151,8 @@ def test_gemm_argument_errors(lib):
     assert b(A16, A16, 4, 64, 128, 7.0, A16, 1, 0, NULL, NULL, S) == -1
     assert b(A16, A16, 4, 64, 128, 7.0, A16, 1, 0, A2, NULL, S) == -3
     assert b(A16, A16, 0, 64, 128, 0.0, A16, 1, 0, NULL, NULL, S) == 0         # gu ignores L
+    t = lib.moe_l1_gemm_wait_selftest
+    # (x, w1, rows, H, I, offsets, E, packed, sf, status, wait_cycles, stream)
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, NULL, 10 ** 7, S) == -1   # status required
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10, S) == -4         # limit out of range
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10 ** 12, S) == -4

@@ -180,3 +180,25 @@ def test_bf16_outputs_of_the_unfused_flows(name):
         hi = W.bf16_bits(np.float32(yv * (1 + parity.GEMM_Y_REL_TOL)))
         assert lo != hi and sw[r0 + r, c] in (lo, hi), (r, c, yv)
     assert bad.shape[0] <= max(2, 1e-4 * want.size)
+
+
+def test_expired_wait_reports_its_status_and_the_device_stays_usable():
+    """Failure path without a fault: with its loads withheld, the kernel's
+    first MMA wait can never complete; after the given limit (~10 ms here)
+    it records the code of the expired wait, every role stops, the TMEM is
+    released, and packed / sf stay untouched. The next GEMM on the same
+    device (which must allocate the TMEM again) is correct."""
+    w = _case("tiny")
+    x, w1, off = dev(w.x), dev(w.w1), torch.from_numpy(w.offsets).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = torch.full((w.rows, w.I // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    ss = torch.full((w.rows, w.I // 16), 0x5A, dtype=torch.uint8, device="cuda")
+    M.moe_l1_gemm_wait_selftest(x, w1, off, status, 20_000_000, sp, ss)
+    code = int(host(status)[0])
+    assert code in (3, 4), code
+    assert bool((sp == 0xA5).all()) and bool((ss == 0x5A).all())
+    status.zero_()
+    p, s, acc = _run(w)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    y_ref = oracle.gemm_swiglu_values(acc[r0:r1].astype(np.float64), w.clamp_L)
+    parity.compare_gemm_fused(p[r0:r1], s[r0:r1], y_ref)
