@@ -350,6 +350,104 @@ def cpu_baseline(w, budget_s: float = 12.0):
             "rows_per_s": n / secs}
 
 
+def _oracle_rows_worker(job):
+    """One row partition of the oracle run (a spawned process; the input is
+    read from shared memory). Returns the seconds spent in the oracle."""
+    shm_name, shape, kind, width, clamp_L, r0, r1 = job
+    from multiprocessing import shared_memory
+    sys.path.insert(0, ROOT)
+    import oracle
+    shm = shared_memory.SharedMemory(name=shm_name)
+    try:
+        data = np.ndarray(shape, dtype=np.uint16, buffer=shm.buf)
+        rows = np.ascontiguousarray(data[r0:r1])
+        t = time.perf_counter()
+        if kind == "quantize":
+            oracle.quantize_nvfp4(rows)
+        else:
+            oracle.swiglu_quantize_nvfp4(rows, clamp_L)
+        return time.perf_counter() - t
+    finally:
+        shm.close()
+
+
+def _oracle_warm(_):
+    sys.path.insert(0, ROOT)
+    import oracle
+    oracle.build()
+    return os.getpid()
+
+
+def cpu_baseline_all_cores(w):
+    """The same oracle over contiguous row partitions of every active row,
+    one spawned process per host core (the input shared, not copied);
+    wall time of the parallel region after the pool has started."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    r0 = 0 if w.offsets is None else int(w.offsets[0])
+    r1 = w.rows if w.offsets is None else int(w.offsets[-1])
+    per_row = (2 * w.width if w.kind == "quantize" else 4 * w.width) + w.width // 2 + w.width // 16
+    shm = shared_memory.SharedMemory(create=True, size=w.data.nbytes)
+    try:
+        np.ndarray(w.data.shape, dtype=np.uint16, buffer=shm.buf)[...] = w.data
+        bounds = np.linspace(r0, r1, cores + 1).astype(np.int64)
+        jobs = [(shm.name, w.data.shape, w.kind, w.width, w.clamp_L, int(a), int(b))
+                for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        with mp.get_context("spawn").Pool(len(jobs)) as pool:
+            pool.map(_oracle_warm, range(len(jobs)))
+            t = time.perf_counter()
+            pool.map(_oracle_rows_worker, jobs)
+            secs = time.perf_counter() - t
+    finally:
+        shm.close()
+        shm.unlink()
+    return {"value": per_row * (r1 - r0) / secs / 1e9, "unit": UNIT, "cores": len(jobs), "kind": "oracle",
+            "sample": f"all {r1 - r0} active rows of the {w.name} workload (I={w.width}) over "
+                      f"{len(jobs)} processes, {secs:.2f} s wall",
+            "rows_per_s": (r1 - r0) / secs}
+
+
+def small_config_extras(torch, lib, W, name: str, stream, per_cold):
+    """The small configs fit in L2 and a single cold launch is latency-bound;
+    beside its cold per-launch percentiles, the hot-L2 back-to-back mean and
+    a CUDA graph of 100 launches, each labelled."""
+    w = W.make(name)
+    srcs, packed, sf, off = device_buffers(w, torch, 1)
+    call = make_call(lib, w, srcs[0], packed, sf, off, stream)
+    with torch.cuda.stream(stream):
+        _, per_hot, _, _ = time_steps(torch, [call], 200, 20, stream)
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(100):
+            call()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    graph_us = e0.elapsed_time(e1) * 1e3 / 1000
+    q = np.percentile(np.asarray(per_cold) * 1e6, [10, 50, 90])
+    nbytes = w.algorithmic_bytes()
+    return {"cold_launch_us_p10_p50_p90": [round(float(v), 2) for v in q],
+            "hot_l2_back_to_back_us": round(statistics.fmean(per_hot) * 1e6, 2),
+            "hot_l2_gbs": round(nbytes / statistics.fmean(per_hot) / 1e9, 1),
+            "cuda_graph_100_launches_us_per_launch": round(graph_us, 2),
+            "cuda_graph_gbs": round(nbytes / (graph_us * 1e-6) / 1e9, 1),
+            "note": "hot-L2 and graph numbers reuse one input resident in L2 (not an HBM measurement)"}
+
+
 def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str, traffic):
     mean_s = statistics.fmean(per_launch_s)
     achieved = bytes_per_launch / mean_s / 1e9
@@ -634,6 +732,8 @@ def main_ours(args):
                 "launch_us_mean": round(mean_s * 1e6, 2),
                 "l2": "flushed before every launch" if cold else "inputs larger than L2",
             }
+            if cold:
+                others[name].update(small_config_extras(torch, lib, W, name, stream, per_o))
 
     extensions = {}
     if not args.no_extra:
@@ -645,6 +745,7 @@ def main_ours(args):
                 extensions["compact_flow"]["launch_us_mean"] / (agg["ms_per_step"] * 1e3), 3)
 
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu_all = cpu_baseline_all_cores(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
         return
     line = {
@@ -661,6 +762,7 @@ def main_ours(args):
         "rows_per_s": round(agg["rows_per_s"], 1),
         "roofline": roof,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
