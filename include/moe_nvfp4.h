@@ -233,7 +233,7 @@ MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_counted(const uint16_t *gu, int64_t 
  *            elsewhere on the device); untouched otherwise. May be NULL.
  * Uses every SM (one CTA each, ~206 KB of shared memory and all 512 TMEM
  * columns of the SM), tcgen05 tensor cores and TMA. Allocates nothing.
- * Returns the codes above; MOE_NVFP4_ELAUNCH also when the driver's
+ * Returns the codes above; MOE_NVFP4_ELAUNCH also when the CUDA driver's
  * tensor-map encoder is unavailable or rejects the tensors.
  * ------------------------------------------------------------------------- */
 MOE_NVFP4_API int moe_l1_gemm_swiglu_nvfp4(const uint16_t *x, const uint16_t *w1, int64_t rows,
