@@ -267,6 +267,30 @@ MOE_NVFP4_API int moe_l1_gemm_bf16(const uint16_t *x, const uint16_t *w1, int64_
                                    int32_t num_experts, int32_t output, uint16_t *out, int32_t *status,
                                    moe_nvfp4_stream_t stream);
 
+/* The same fused L1 GEMM with NVFP4 weights:
+ *   w1_packed  uint8 [num_experts, 2I, H/2]: two E2M1 nibbles per byte along
+ *              K, even k in the low nibble -- the layout moe_nvfp4_quantize
+ *              writes for a BF16 [num_experts * 2I, H] weight matrix
+ *   w1_sf      uint8 [num_experts, 2I, H/16]: E4M3 codes, one per 16 along K
+ * The kernel expands each weight tile to BF16 in shared memory (exactly:
+ * e2m1 * e4m3 has at most 6 significant bits), so its outputs equal those
+ * of moe_l1_gemm_swiglu_nvfp4 on the dequantized weights bit for bit, while
+ * a weight costs 0.5625 bytes of HBM traffic instead of 2. H % 256 == 0;
+ * both weight pointers 16-byte aligned; other arguments as above. Wait
+ * codes in `status` also include 5 (MMA issuer / expanded weight tile),
+ * 6 (expanders / loaded stage) and 7 (expanders / free expanded tile). */
+MOE_NVFP4_API int moe_l1_gemm_w4_swiglu_nvfp4(const uint16_t *x, const uint8_t *w1_packed,
+                                              const uint8_t *w1_sf, int64_t rows, int64_t H, int64_t I,
+                                              float clamp_L, const int32_t *expert_offsets,
+                                              int32_t num_experts, uint8_t *packed, uint8_t *sf,
+                                              int32_t *status, moe_nvfp4_stream_t stream);
+
+/* Diagnostic: the fp32 accumulators [rows, 2I] of moe_l1_gemm_w4_swiglu_nvfp4. */
+MOE_NVFP4_API int moe_l1_gemm_w4_accumulators(const uint16_t *x, const uint8_t *w1_packed,
+                                              const uint8_t *w1_sf, int64_t rows, int64_t H, int64_t I,
+                                              const int32_t *expert_offsets, int32_t num_experts,
+                                              float *acc, int32_t *status, moe_nvfp4_stream_t stream);
+
 /* Diagnostic of the failure path: moe_l1_gemm_swiglu_nvfp4's kernel with
  * its loads withheld (nothing ever completes the first stage) and every
  * internal wait limited to wait_cycles SM clock cycles (1000 ..

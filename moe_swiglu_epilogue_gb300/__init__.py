@@ -21,7 +21,7 @@ __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_v
            "moe_swiglu_nvfp4_quantize_ex", "moe_swiglu_bf16", "moe_nvfp4_dequantize",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
            "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators", "moe_l1_gemm_bf16",
-           "moe_l1_gemm_wait_selftest",
+           "moe_l1_gemm_wait_selftest", "moe_l1_gemm_w4_swiglu_nvfp4", "moe_l1_gemm_w4_accumulators",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
 
 _lib = None
@@ -81,6 +81,10 @@ def load_library():
     lib.moe_l1_gemm_swiglu_nvfp4.restype = ctypes.c_int
     lib.moe_l1_gemm_accumulators.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P]
     lib.moe_l1_gemm_accumulators.restype = ctypes.c_int
+    lib.moe_l1_gemm_w4_swiglu_nvfp4.argtypes = [P, P, P, I64, I64, I64, F, P, I32, P, P, P, P]
+    lib.moe_l1_gemm_w4_swiglu_nvfp4.restype = ctypes.c_int
+    lib.moe_l1_gemm_w4_accumulators.argtypes = [P, P, P, I64, I64, I64, P, I32, P, P, P]
+    lib.moe_l1_gemm_w4_accumulators.restype = ctypes.c_int
     lib.moe_l1_gemm_wait_selftest.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P, I64, P]
     lib.moe_l1_gemm_wait_selftest.restype = ctypes.c_int
     lib.moe_l1_gemm_bf16.argtypes = [P, P, I64, I64, I64, F, P, I32, I32, P, P, P]
@@ -428,3 +432,54 @@ def moe_l1_gemm_wait_selftest(x, w1, expert_offsets, status, wait_cycles: int, p
             _stream_ptr(stream))
     _check(rc, "moe_l1_gemm_wait_selftest")
     return packed, sf
+
+
+def _w4_operands(x, w1_packed, w1_sf, expert_offsets):
+    torch = _torch()
+    x = _bf16_bits(x, "x", 256)
+    rows, H = x.shape
+    for t, name in ((w1_packed, "w1_packed"), (w1_sf, "w1_sf")):
+        if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor [experts, 2I, ...]")
+    E, two_i, half = w1_packed.shape
+    if half * 2 != H or tuple(w1_sf.shape) != (E, two_i, H // 16) or two_i % 256:
+        raise ValueError("w1_packed must be [E, 2I, H/2] and w1_sf [E, 2I, H/16], 2I % 256 == 0")
+    if expert_offsets is None or expert_offsets.dtype != torch.int32 or not expert_offsets.is_cuda \
+            or tuple(expert_offsets.shape) != (E + 1,):
+        raise ValueError(f"expert_offsets must be an int32 CUDA tensor of shape ({E + 1},)")
+    return x, E, two_i // 2, H
+
+
+def moe_l1_gemm_w4_swiglu_nvfp4(x, w1_packed, w1_sf, clamp_L: float, expert_offsets, packed=None, sf=None,
+                                status=None, stream=None):
+    """The fused L1 GEMM with NVFP4 weights (packed nibbles [E, 2I, H/2] and
+    E4M3 scales [E, 2I, H/16], as moe_nvfp4_quantize lays them out)."""
+    x, E, I, H = _w4_operands(x, w1_packed, w1_sf, expert_offsets)
+    rows = x.shape[0]
+    packed = _out(packed, (rows, I // 2), x.device, "packed")
+    sf = _out(sf, (rows, I // 16), x.device, "sf")
+    with _torch().cuda.device(x.device):
+        rc = load_library().moe_l1_gemm_w4_swiglu_nvfp4(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1_packed.data_ptr()),
+            ctypes.c_void_p(w1_sf.data_ptr()), rows, H, I, float(clamp_L),
+            ctypes.c_void_p(expert_offsets.data_ptr()), E, ctypes.c_void_p(packed.data_ptr()),
+            ctypes.c_void_p(sf.data_ptr()), ctypes.c_void_p(0 if status is None else status.data_ptr()),
+            _stream_ptr(stream))
+    _check(rc, "moe_l1_gemm_w4_swiglu_nvfp4")
+    return packed, sf
+
+
+def moe_l1_gemm_w4_accumulators(x, w1_packed, w1_sf, expert_offsets, acc=None, status=None, stream=None):
+    torch = _torch()
+    x, E, I, H = _w4_operands(x, w1_packed, w1_sf, expert_offsets)
+    rows = x.shape[0]
+    if acc is None:
+        acc = torch.zeros((rows, 2 * I), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = load_library().moe_l1_gemm_w4_accumulators(
+            ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1_packed.data_ptr()),
+            ctypes.c_void_p(w1_sf.data_ptr()), rows, H, I, ctypes.c_void_p(expert_offsets.data_ptr()), E,
+            ctypes.c_void_p(acc.data_ptr()), ctypes.c_void_p(0 if status is None else status.data_ptr()),
+            _stream_ptr(stream))
+    _check(rc, "moe_l1_gemm_w4_accumulators")
+    return acc

@@ -156,3 +156,10 @@ def test_gemm_argument_errors(lib):
     assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, NULL, 10 ** 7, S) == -1   # status required
     assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10, S) == -4         # limit out of range
     assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10 ** 12, S) == -4
+    w4 = lib.moe_l1_gemm_w4_swiglu_nvfp4
+    # (x, w1_packed, w1_sf, rows, H, I, clamp_L, offsets, E, packed, sf, status, stream)
+    assert w4(A16, A16, A16, 4, 128, 128, 7.0, A16, 1, A16, A16, NULL, S) == -2   # H % 256
+    assert w4(A16, NULL, A16, 4, 256, 128, 7.0, A16, 1, A16, A16, NULL, S) == -1
+    assert w4(A16, A16, A2, 4, 256, 128, 7.0, A16, 1, A16, A16, NULL, S) == -3
+    assert w4(A16, A16, A16, 4, 256, 128, 0.0, A16, 1, A16, A16, NULL, S) == -5
+    assert w4(NULL, NULL, NULL, 0, 256, 128, 7.0, A16, 1, NULL, NULL, NULL, S) == 0

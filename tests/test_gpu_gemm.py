@@ -202,3 +202,68 @@ def test_expired_wait_reports_its_status_and_the_device_stays_usable():
     r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
     y_ref = oracle.gemm_swiglu_values(acc[r0:r1].astype(np.float64), w.clamp_L)
     parity.compare_gemm_fused(p[r0:r1], s[r0:r1], y_ref)
+
+
+def _w4_case(name):
+    """The case's BF16 weights quantized to NVFP4 by the oracle, and the
+    oracle's (exact) dequantization of them back to BF16."""
+    w = _case(name)
+    E, two_i, H = w.w1.shape
+    qp, qs = oracle.quantize_nvfp4(w.w1.reshape(E * two_i, H))
+    deq = oracle.dequantize_nvfp4(qp, qs)
+    return w, qp.reshape(E, two_i, H // 2), qs.reshape(E, two_i, H // 16), deq.reshape(E, two_i, H)
+
+
+def _run_w4(w, qp, qs):
+    x, off = dev(w.x), torch.from_numpy(w.offsets).cuda()
+    tq, ts = torch.from_numpy(qp).cuda(), torch.from_numpy(qs).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sp = torch.full((w.rows, w.I // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    ss = torch.full((w.rows, w.I // 16), 0x5A, dtype=torch.uint8, device="cuda")
+    p, s = M.moe_l1_gemm_w4_swiglu_nvfp4(x, tq, ts, w.clamp_L, off, sp, ss, status)
+    acc = M.moe_l1_gemm_w4_accumulators(x, tq, ts, off, status=status)
+    assert int(host(status)[0]) == 0
+    return host(p), host(s), host(acc)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_w4_gemm_equals_the_bf16_gemm_on_the_dequantized_weights(name):
+    """NVFP4 weights expanded in the kernel: the outputs and accumulators
+    equal, bit for bit, the BF16 GEMM's on the oracle's dequantization."""
+    w, qp, qs, deq = _w4_case(name)
+    p4, s4, a4 = _run_w4(w, qp, qs)
+    wd = W.GemmWorkload(w.name, w.rows, w.H, w.I, w.x, deq, w.offsets, w.clamp_L)
+    p, s, a = _run(wd)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    assert np.array_equal(a4[r0:r1], a[r0:r1])
+    assert np.array_equal(p4, p) and np.array_equal(s4, s)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_w4_gemm_against_the_oracle(name):
+    w, qp, qs, deq = _w4_case(name)
+    p, s, acc = _run_w4(w, qp, qs)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    ref = oracle.l1_gemm_accumulators(w.x, deq, w.offsets)[r0:r1]
+    mag = oracle.l1_gemm_abs_accumulators(w.x, deq, w.offsets)[r0:r1]
+    assert np.all(np.abs(acc[r0:r1] - ref) <= acc_bound(w.H) * mag + 1e-30)
+    y_ref = oracle.gemm_swiglu_values(acc[r0:r1].astype(np.float64), w.clamp_L)
+    parity.compare_gemm_fused(p[r0:r1], s[r0:r1], y_ref)
+    assert np.all(p[r1:] == 0xA5) and np.all(s[r1:] == 0x5A)
+
+
+def test_w4_gemm_full_width():
+    """H = 7168, I = 2048 over 4 experts: equal to the BF16 GEMM on the
+    dequantized weights everywhere; sampled rows against the oracle."""
+    w = W.gemm_ragged(tokens=256, experts=4, topk=2, H=7168, I=2048, seed=22)
+    E, two_i, H = w.w1.shape
+    qp, qs = oracle.quantize_nvfp4(w.w1.reshape(E * two_i, H))
+    deq = oracle.dequantize_nvfp4(qp, qs).reshape(E, two_i, H)
+    p4, s4, a4 = _run_w4(w, qp.reshape(E, two_i, H // 2), qs.reshape(E, two_i, H // 16))
+    p, s, a = _run(W.GemmWorkload(w.name, w.rows, H, w.I, w.x, deq, w.offsets, w.clamp_L))
+    assert np.array_equal(a4, a) and np.array_equal(p4, p) and np.array_equal(s4, s)
+    rows = np.sort(np.random.default_rng(4).choice(np.arange(int(w.offsets[-1])), 16, replace=False))
+    sub_off = np.searchsorted(rows, w.offsets).astype(np.int32)
+    ref = oracle.l1_gemm_accumulators(w.x[rows], deq, sub_off)
+    mag = oracle.l1_gemm_abs_accumulators(w.x[rows], deq, sub_off)
+    assert np.all(np.abs(a4[rows] - ref) <= acc_bound(H) * mag + 1e-30)
