@@ -567,15 +567,18 @@ def gemm_measurements(torch, lib, M, W, stream, hbm_peak: float, cases=GEMM_CASE
             tflops_peak = float(json.load(fh).get("bf16_tflops") or 0) or None
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     res = {}
-    w1, w1_experts = None, None
+    w1 = wq = ws = w1_experts = None
     for name, E, tokens, steps in cases:
         if w1_experts != E:
-            w1 = None
+            w1 = wq = ws = None
             torch.cuda.empty_cache()
             w1_np = W.gemm_weights(E, H, I)
             w1 = torch.from_numpy(w1_np.view(np.int16)).cuda()
             w1_experts = E
             del w1_np
+            # the same weights in NVFP4 (our quantize-only kernel writes the layout the GEMM reads)
+            wq, ws = M.moe_nvfp4_quantize(w1.view(E * 2 * I, H), stream=stream)
+            torch.cuda.synchronize()
         x_np, offsets = W.gemm_rows(tokens, E, 8, H)
         x = torch.from_numpy(x_np.view(np.int16)).cuda()
         off = torch.from_numpy(offsets).cuda()
@@ -595,6 +598,21 @@ def gemm_measurements(torch, lib, M, W, stream, hbm_peak: float, cases=GEMM_CASE
         active_experts = int(np.count_nonzero(np.diff(offsets.astype(np.int64)) > 0))
         nbytes = active_rows * (2 * H + I // 2 + I // 16) + active_experts * 2 * I * H * 2
         flops = 2 * active_rows * H * 2 * I
+        call4 = DirectCall(lib.moe_l1_gemm_w4_swiglu_nvfp4,
+                           (P(x.data_ptr()), P(wq.data_ptr()), P(ws.data_ptr()), rows, H, I, ctypes.c_float(7.0),
+                            P(off.data_ptr()), ctypes.c_int32(E), P(pk.data_ptr()), P(sc.data_ptr()),
+                            P(status.data_ptr()), s))
+        with torch.cuda.stream(stream):
+            _, per4, _, _ = time_steps(torch, [call4], steps, warmup, stream)
+        w4_s = statistics.fmean(per4)
+        nbytes4 = active_rows * (2 * H + I // 2 + I // 16) + active_experts * 2 * I * (H // 2 + H // 16)
+        entry["w4_nvfp4_weights"] = {
+            "launch_us_mean": round(w4_s * 1e6, 1), "bytes": nbytes4,
+            "gbs": round(nbytes4 / w4_s / 1e9, 1), "frac_of_hbm_peak": round(nbytes4 / w4_s / 1e9 / hbm_peak, 4),
+            "tflops": round(flops / w4_s / 1e12, 1),
+            "frac_of_bf16_peak": None if tflops_peak is None else round(flops / w4_s / 1e12 / tflops_peak, 4),
+            "vs_bf16_weights_time": round(w4_s / fused_s, 3),
+            "what": "moe_l1_gemm_w4_swiglu_nvfp4: the same weights quantized to NVFP4 (0.5625 B each)"}
         res[name] = entry
         entry.update({
             "launch_us_mean": round(fused_s * 1e6, 1),
@@ -667,7 +685,7 @@ def gemm_measurements(torch, lib, M, W, stream, hbm_peak: float, cases=GEMM_CASE
         torch.cuda.empty_cache()
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "a GEMM wait expired"
-    del w1
+    del w1, wq, ws
     torch.cuda.empty_cache()
     return res
 

@@ -455,11 +455,14 @@ done:
 // The same GEMM with NVFP4 weights (BF16 activations). The weights arrive as
 // packed E2M1 nibbles [E, 2I, H/2] with one E4M3 scale per 16 along K
 // [E, 2I, H/16] -- the layout moe_nvfp4_quantize writes -- so a weight tile
-// costs 0.5625 bytes per element in HBM instead of 2. Four converter warps
-// expand each stage in shared memory into the BF16 tile the MMA reads, in
-// the layout a 128-byte-swizzled TMA load would give; e2m1 * e4m3 has at
-// most 6 significant bits, so the expansion is exact, and the result equals
-// the BF16 GEMM on the dequantized weights bit for bit.
+// costs 0.5625 bytes per element in HBM instead of 2. Eight expander warps
+// turn each stage in shared memory into the BF16 tile the MMA reads, in the
+// layout a 128-byte-swizzled TMA load would give; e2m1 * e4m3 has at most 6
+// significant bits, so the expansion is exact, and the result equals the
+// BF16 GEMM on the dequantized weights bit for bit. The expansion adds a
+// 32 KB shared-memory write and an 8 KB read to every stage, which makes
+// shared-memory bandwidth, not HBM, the bound: the kernel saves weight
+// memory and HBM traffic, not time, against the BF16-weight kernel.
 // ---------------------------------------------------------------------------
 
 constexpr int kW4RawStages = 4;                          // x tile + packed weight tile
@@ -468,8 +471,8 @@ constexpr uint32_t kW4FpBytes = kBN * kBK / 2;           // 8 KB of nibbles per 
 constexpr uint32_t kW4RawBytes = kStageA + kW4FpBytes;   // 24 KB
 constexpr uint32_t kW4ScaleBytes = kBN * 16;             // scales of 4 stages: 16 per row
 constexpr int kW4ScaleSlots = 2;
-constexpr int kW4ConvThreads = 128;
-constexpr int kW4Threads = kGemmThreads + kW4ConvThreads;   // warps 6-9 expand the weights
+constexpr int kW4ConvThreads = 256;
+constexpr int kW4Threads = kGemmThreads + kW4ConvThreads;   // warps 6-13 expand the weights
 
 struct W4Shared {
     uint64_t full[kW4RawStages];       // x + nibbles (+ scales every 4th stage) landed
@@ -624,7 +627,7 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             tmem_fence_before();
             mbar_arrive(&S.acc_empty[b]);
         }
-    } else {                                                        // weight expanders, warps 6-9
+    } else {                                                        // weight expanders, warps 6-13
         const int ct = threadIdx.x - kGemmThreads;
         const int64_t iters = tiles_of_cta(total) * nkb;
         for (int64_t it = 0; it < iters; it++) {
