@@ -768,8 +768,11 @@ def main_ours(args):
     kernel = "nvfp4_quantize_kernel" if w.kind == "quantize" else "swiglu_nvfp4_kernel"
     roof = roofline(w.algorithmic_bytes(), per, peak, peak_src, recorded_traffic(kernel, w.name))
 
+    # the extra measurements (other workloads, extensions, the L1 GEMM with
+    # 15 GB of weights per process) run in single-GPU runs only
+    extras = not args.no_extra and world == 1
     others = {}
-    if not args.no_extra:
+    if extras:
         for name, cold in (("fused", True), ("prefill", False), ("quantize", True),
                            ("prefill_quantize", False)):
             if name == args.workload:
@@ -792,7 +795,7 @@ def main_ours(args):
                 others[name].update(small_config_extras(torch, lib, W, name, stream, per_o))
 
     extensions = {}
-    if not args.no_extra:
+    if extras:
         extensions = extension_measurements(torch, lib, M, W, stream, min(args.steps, 200),
                                             min(args.warmup, 20), peak)
         extensions.update(gemm_measurements(torch, lib, M, W, stream, peak))
