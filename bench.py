@@ -773,7 +773,7 @@ def main_ours(args):
     extras = not args.no_extra and world == 1
     others = {}
     if extras:
-        for name, cold in (("fused", True), ("prefill", False), ("quantize", True),
+        for name, cold in (("fused", True), ("prefill", False), ("edge", False), ("quantize", True),
                            ("prefill_quantize", False)):
             if name == args.workload:
                 continue
