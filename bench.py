@@ -95,9 +95,11 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the activation-step kernels are compiled from (the
+    C header holds declarations only)."""
     h = hashlib.sha256()
     for rel in ("moe_swiglu_epilogue_gb300/csrc/moe_nvfp4.cu",
-                "moe_swiglu_epilogue_gb300/csrc/nvfp4_device.cuh", "include/moe_nvfp4.h"):
+                "moe_swiglu_epilogue_gb300/csrc/nvfp4_device.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
