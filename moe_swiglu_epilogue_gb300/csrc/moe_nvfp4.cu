@@ -636,7 +636,15 @@ __device__ __forceinline__ int segment_of(const int32_t* offsets, int E, int64_t
     return lo;
 }
 
-template <int kMode, bool kBf16Clamp>
+// A thread's current segment for padded output, in blocks (row r starts at
+// block r * bpr, so row >= R exactly when block >= R * bpr): the first
+// block past the segment, the blocks [lo, hi) whose output row lies inside
+// [0, out_rows), and the output block minus the input block.
+struct alignas(32) PadSegment {
+    int64_t end_blk, lo_blk, hi_blk, shift_blk;
+};
+
+template <int kMode, bool kBf16Clamp, bool kPadded>
 __global__ void __launch_bounds__(kThreads, kMinBlocksFused)
 swiglu_ex_kernel(const ExArgs X) {
     wait_for_preceding_grid();
@@ -652,11 +660,19 @@ swiglu_ex_kernel(const ExArgs X) {
     per_cta = (per_cta + kChunk - 1) / kChunk * kChunk;
     const int64_t cta_begin = b0 + static_cast<int64_t>(blockIdx.x) * per_cta;
     const int64_t cta_end = cta_begin + per_cta < b1 ? cta_begin + per_cta : b1;
-    const bool padded = (kMode != kExCompact) && X.out_offsets != nullptr && A.offsets != nullptr;
+    const bool padded = kPadded && X.out_offsets != nullptr && A.offsets != nullptr;
+    // padded output: each thread's current segment (and its index) lives in
+    // shared memory and is read at the store, so nothing of it is live
+    // across the arithmetic
     __shared__ int next_chunk;
+    __shared__ PadSegment pad_seg[kThreads];
+    __shared__ int32_t pad_e[kThreads];
     if (threadIdx.x == 0) next_chunk = 0;
+    if (padded) {
+        pad_seg[threadIdx.x] = PadSegment{-1, 0, 0, 0};
+        pad_e[threadIdx.x] = -1;
+    }
     __syncthreads();
-    int seg_cursor = -1;        // lane 0: segment of this warp's previous chunk
     for (;;) {                                              // warp-uniform
         int c = 0;
         if (lane == 0) c = atomicAdd(&next_chunk, 1);
@@ -676,62 +692,47 @@ swiglu_ex_kernel(const ExArgs X) {
                 for (int j = 0; j < 16; j++) w[k][j] = 0u;
             }
         }
-        // padded output (while the loads are in flight): the chunk's first
-        // row and column, that row's segment, where it ends and its row
-        // shift. A warp's chunks only move forward, so the segment is found
-        // by stepping on from the previous chunk's, or by bisection.
-        int64_t r0 = 0, c0 = 0, seg_end = 0, shift0 = 0;
-        int e0 = 0;
-        if (padded) {
-            if (lane == 0) {
-                r0 = base / A.bpr;
-                c0 = base - r0 * A.bpr;
-                int e = seg_cursor;
-                for (int t = 0; e >= 0 && t < 4 && e + 1 < A.E &&
-                                r0 >= static_cast<int64_t>(__ldg(A.offsets + e + 1)); t++)
-                    e++;
-                if (e < 0 || (e + 1 < A.E && r0 >= static_cast<int64_t>(__ldg(A.offsets + e + 1))))
-                    e = segment_of(A.offsets, A.E, r0);
-                seg_cursor = e0 = e;
-                seg_end = __ldg(A.offsets + e0 + 1);
-                shift0 = static_cast<int64_t>(__ldg(X.out_offsets + e0)) - __ldg(A.offsets + e0);
-            }
-            r0 = __shfl_sync(kFullMask, r0, 0);
-            c0 = __shfl_sync(kFullMask, c0, 0);
-            e0 = __shfl_sync(kFullMask, e0, 0);
-            seg_end = __shfl_sync(kFullMask, seg_end, 0);
-            shift0 = __shfl_sync(kFullMask, shift0, 0);
-        }
-        // output block of block k: its padded position and whether it is stored
-        auto out_block = [&](int k, int64_t blk, bool valid, int64_t& oblk, bool& store) {
+        // output block of block blk: its padded position and whether it is
+        // stored (called by the whole warp after the block's arithmetic)
+        auto out_block = [&](int64_t blk, bool valid, int64_t& oblk, bool& store) {
             oblk = blk;
             store = valid;
-            if (padded && valid) {
-                const int64_t j = c0 + 32 * k + lane;
-                const int64_t row = r0 + (A.bpr >= kChunk ? (j >= A.bpr ? 1 : 0) : j / A.bpr);
-                int64_t shift = shift0;
-                if (row >= seg_end) {                       // past the chunk's first segment
-                    int e = e0;
-                    while (e + 1 < A.E && row >= static_cast<int64_t>(__ldg(A.offsets + e + 1))) e++;
-                    shift = static_cast<int64_t>(__ldg(X.out_offsets + e)) - __ldg(A.offsets + e);
-                }
-                const int64_t orow = row + shift;
-                store = orow >= 0 && orow < X.out_rows;
-                oblk = blk + shift * A.bpr;
+            if (!padded) return;
+            PadSegment sg = pad_seg[threadIdx.x];
+            if (valid && blk >= sg.end_blk) {               // once per segment
+                // a thread's blocks only move forward: step on from its
+                // segment, else bisect
+                int e = pad_e[threadIdx.x];
+                const int64_t row = blk / A.bpr;
+                for (int t = 0; e >= 0 && t < 4 && e + 1 < A.E && row >= __ldg(A.offsets + e + 1); t++)
+                    e++;
+                if (e < 0 || (e + 1 < A.E && row >= __ldg(A.offsets + e + 1)))
+                    e = segment_of(A.offsets, A.E, row);
+                // rows are int32, so the stored-row range is clamped to [0, 2^31]
+                const int64_t shift = static_cast<int64_t>(__ldg(X.out_offsets + e)) - __ldg(A.offsets + e);
+                const int64_t lo = -shift, hi = X.out_rows - shift, top = int64_t(1) << 31;
+                sg.end_blk = static_cast<int64_t>(__ldg(A.offsets + e + 1)) * A.bpr;
+                sg.lo_blk = (lo < 0 ? 0 : (lo > top ? top : lo)) * A.bpr;
+                sg.hi_blk = (hi < 0 ? 0 : (hi > top ? top : hi)) * A.bpr;
+                sg.shift_blk = shift * A.bpr;
+                pad_seg[threadIdx.x] = sg;
+                pad_e[threadIdx.x] = e;
             }
+            store = valid && blk >= sg.lo_blk && blk < sg.hi_blk;
+            oblk = blk + sg.shift_blk;
         };
         if (kMode == kExQuantize) {
 #pragma unroll
             for (int k = 0; k < kUnroll; k++) {
                 const int64_t blk = base + 32 * k + lane;
                 const bool valid = blk < cta_end;
-                int64_t oblk;
-                bool store;
-                out_block(k, blk, valid, oblk, store);
                 float y[16];
                 fast_swiglu16<kBf16Clamp>(A, w[k], y);
                 uint32_t lo, hi, code;
                 scaled_block(X, A.gu + blk * 32, valid, y, lo, hi, code);
+                int64_t oblk;
+                bool store;
+                out_block(blk, valid, oblk, store);
                 if (store) {
                     *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
                     A.sf[oblk] = static_cast<uint8_t>(code);
@@ -762,9 +763,6 @@ swiglu_ex_kernel(const ExArgs X) {
                         dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
                     }
                 } else {                                // compat: quantize the BF16 values
-                    int64_t oblk;
-                    bool store;
-                    out_block(k, blk, valid, oblk, store);
                     float v[16];
                     uint32_t lo, hi, code;
                     if (kMode == kExCompatUnit) {               // BF16 values: the cheap exact form
@@ -773,7 +771,7 @@ swiglu_ex_kernel(const ExArgs X) {
                             v[2 * q] = bf16_lo(b[q]);
                             v[2 * q + 1] = bf16_hi(b[q]);
                         }
-                        code = quantize16_exact<false, false>(v, lo, hi);
+                        code = quantize16_exact<false, true>(v, lo, hi);
                     } else {
 #pragma unroll
                         for (int q = 0; q < 8; q++) {
@@ -782,6 +780,9 @@ swiglu_ex_kernel(const ExArgs X) {
                         }
                         code = quantize16_exact<true, true>(v, lo, hi);
                     }
+                    int64_t oblk;
+                    bool store;
+                    out_block(blk, valid, oblk, store);
                     if (store) {
                         *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
                         A.sf[oblk] = static_cast<uint8_t>(code);
@@ -944,7 +945,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int occ[2][3] = {{0, 0, 0}, {0, 0, 0}};   // [bf16 clamp][plain, counted, values]
-    int occ_ex[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // [bf16 clamp][ExMode]
+    int occ_ex[2][7] = {};          // [bf16 clamp][ExMode, then padded kExQuantize, kExCompat, kExCompatUnit]
     int occ_quant[2] = {0, 0};                  // [scaled]
     int occ_dequant = 0;
 };
@@ -964,13 +965,19 @@ bool fused_occupancy(int* occ) {
 template <bool kBf16Clamp>
 bool ex_occupancy(int* occ) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-               &occ[0], swiglu_ex_kernel<kExQuantize, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+               &occ[0], swiglu_ex_kernel<kExQuantize, kBf16Clamp, false>, kThreads, 0) == cudaSuccess &&
            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-               &occ[1], swiglu_ex_kernel<kExCompat, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+               &occ[1], swiglu_ex_kernel<kExCompat, kBf16Clamp, false>, kThreads, 0) == cudaSuccess &&
            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-               &occ[2], swiglu_ex_kernel<kExCompact, kBf16Clamp>, kThreads, 0) == cudaSuccess &&
+               &occ[2], swiglu_ex_kernel<kExCompact, kBf16Clamp, false>, kThreads, 0) == cudaSuccess &&
            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-               &occ[3], swiglu_ex_kernel<kExCompatUnit, kBf16Clamp>, kThreads, 0) == cudaSuccess;
+               &occ[3], swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, false>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[4], swiglu_ex_kernel<kExQuantize, kBf16Clamp, true>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[5], swiglu_ex_kernel<kExCompat, kBf16Clamp, true>, kThreads, 0) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+               &occ[6], swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, true>, kThreads, 0) == cudaSuccess;
 }
 
 int device_info(DeviceInfo& out) {
@@ -1135,14 +1142,21 @@ template <bool kBf16Clamp>
 void launch_ex_kernel(const ExArgs& X, int mode, int64_t nblk, const DeviceInfo& di,
                       cudaStream_t stream) {
     const int* occ = di.occ_ex[kBf16Clamp ? 1 : 0];
-    if (mode == kExQuantize)
-        launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp>, grid_for(nblk, di.sms, occ[0]), stream, X);
+    const bool padded = X.out_offsets != nullptr && X.f.offsets != nullptr;
+    if (mode == kExQuantize && padded)
+        launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[4]), stream, X);
+    else if (mode == kExQuantize)
+        launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[0]), stream, X);
+    else if (mode == kExCompat && X.gs == 1.0f && padded)
+        launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[6]), stream, X);
     else if (mode == kExCompat && X.gs == 1.0f)
-        launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp>, grid_for(nblk, di.sms, occ[3]), stream, X);
+        launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[3]), stream, X);
+    else if (mode == kExCompat && padded)
+        launch(swiglu_ex_kernel<kExCompat, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[5]), stream, X);
     else if (mode == kExCompat)
-        launch(swiglu_ex_kernel<kExCompat, kBf16Clamp>, grid_for(nblk, di.sms, occ[1]), stream, X);
+        launch(swiglu_ex_kernel<kExCompat, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[1]), stream, X);
     else
-        launch(swiglu_ex_kernel<kExCompact, kBf16Clamp>, grid_for(nblk, di.sms, occ[2]), stream, X);
+        launch(swiglu_ex_kernel<kExCompact, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[2]), stream, X);
 }
 
 int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_t* offsets,

@@ -107,6 +107,28 @@ def test_padded_segments_bit_exact_and_gaps_untouched(I):
         assert np.any(rp == 0xA5)                          # gaps exist and stayed
 
 
+@pytest.mark.parametrize("I", [16, 48, 2048])
+def test_padded_segments_empty_single_row_and_offset_start(I):
+    """Hand-made segments: a nonzero first offset, empty and single-row
+    segments, a long one; output segments padded to 16 rows with gaps. I = 16
+    and 48 put several rows (and segment ends) inside one 64-block chunk."""
+    offsets = np.array([5, 5, 6, 6, 6, 40, 41, 300, 300, 301, 333], np.int32)
+    w = W.fused_normal(rows=340, I=I, seed=12)
+    counts = np.diff(offsets)
+    out_off = np.concatenate([[3], 3 + np.cumsum((counts + 15) // 16 * 16 + 2)]).astype(np.int32)
+    out_rows = int(out_off[-1]) + 7
+    for gs, compat in ((1.0, False), (1.3, False), (0.9, True)):
+        sent_p = np.full((out_rows, I // 2), 0xA5, np.uint8)
+        sent_s = np.full((out_rows, I // 16), 0x5A, np.uint8)
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(
+            dev(w.data), w.clamp_L, torch.from_numpy(offsets).cuda(), gs, compat,
+            torch.from_numpy(out_off).cuda(), out_rows, torch.from_numpy(sent_p.copy()).cuda(),
+            torch.from_numpy(sent_s.copy()).cuda())
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, w.clamp_L, offsets, out_off, out_rows,
+                                                 gs, compat, packed=sent_p, sf=sent_s)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
+
+
 def test_compact_writer_bit_exact():
     for w in (W.fused_normal(rows=512, I=2048, seed=4), W.prefill_heavy_tail(rows=256, I=3072),
               W.edge_structured(rows=128, I=4096)):
