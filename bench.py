@@ -496,13 +496,18 @@ def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str
             "timing": "mean launch = timed region / launches (back-to-back on one stream)"}
 
 
-def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, peak: float):
+EXTENSION_CASES = ("two_level_scale", "bf16_compat", "bf16_compat_scaled", "padded_segments")
+
+
+def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, peak: float,
+                           only=None):
     """Launch time and algorithmic GB/s of the extensions on the ragged
     workload (dequantization on the prefill quantize-only outputs): the
-    two-level scale, the BF16-compat mode, padded per-expert output (segments
-    padded to 128 rows), the compact BF16 writer, the compact flow (writer +
-    quantize-only of its output, the pages' planned pipeline) and
-    dequantization."""
+    two-level scale, the BF16-compat mode (global scale 1 and 1.25), padded
+    per-expert output (segments padded to 128 rows), the compact BF16 writer,
+    the compact flow (writer + quantize-only of its output, the pages'
+    planned pipeline) and dequantization. `only`: a subset of
+    EXTENSION_CASES, measured alone."""
     P = ctypes.c_void_p
     FO = M.FusedOptions
     w = W.make("ragged")
@@ -513,7 +518,9 @@ def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, pe
     E = off.shape[0] - 1
     packed = torch.empty((rows, I // 2), dtype=torch.uint8, device="cuda")
     sf = torch.empty((rows, I // 16), dtype=torch.uint8, device="cuda")
-    compact = torch.empty((rows, I), dtype=torch.bfloat16, device="cuda")
+    # two compact tensors (the writer alternates between them), so that the
+    # quantize-only leg reads one that is not left in L2 by the previous step
+    compacts = [torch.empty((rows, I), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     counts = np.diff(w.offsets)
     out_off = np.concatenate([[0], np.cumsum(np.ceil(counts / 128).astype(np.int64) * 128)])
     out_rows = int(out_off[-1])
@@ -523,6 +530,7 @@ def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, pe
     opts = {
         "two_level_scale": FO(1.25, 0, None, rows),
         "bf16_compat": FO(1.0, 1, None, rows),
+        "bf16_compat_scaled": FO(1.25, 1, None, rows),
         "padded_segments": FO(1.0, 0, out_off_t.data_ptr(), out_rows),
     }
     fused_bytes = w.algorithmic_bytes()
@@ -540,46 +548,55 @@ def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, pe
                      "what": note}
 
     for name, opt in opts.items():
+        if only is not None and name not in only:
+            continue
         pk, sc = (packed_p, sf_p) if name == "padded_segments" else (packed, sf)
         calls = [DirectCall(lib.moe_swiglu_nvfp4_quantize_ex,
                             (P(x.data_ptr()), rows, I, ctypes.c_float(L), P(off.data_ptr()),
                              ctypes.c_int32(E), ctypes.byref(opt), P(pk.data_ptr()),
                              P(sc.data_ptr()), s)) for x in srcs]
         measure(name, calls, fused_bytes, "moe_swiglu_nvfp4_quantize_ex on the ragged workload")
+    if only is not None:
+        return res
     writer = [DirectCall(lib.moe_swiglu_bf16, (P(x.data_ptr()), rows, I, ctypes.c_float(L),
                                                P(off.data_ptr()), ctypes.c_int32(E),
-                                               P(compact.data_ptr()), s)) for x in srcs]
+                                               P(c.data_ptr()), s)) for x, c in zip(srcs, compacts)]
     measure("compact_writer", writer, writer_bytes, "moe_swiglu_bf16: gate/up -> BF16 [rows, I]")
-    quant = DirectCall(lib.moe_nvfp4_quantize, (P(compact.data_ptr()), rows, I,
-                                                P(packed.data_ptr()), P(sf.data_ptr()), s))
-    measure("quantize_of_compact", [quant], quant_bytes, "moe_nvfp4_quantize of the BF16 tensor")
+    quants = [DirectCall(lib.moe_nvfp4_quantize, (P(c.data_ptr()), rows, I,
+                                                  P(packed.data_ptr()), P(sf.data_ptr()), s))
+              for c in compacts]
+    measure("quantize_of_compact", quants, quant_bytes,
+            "moe_nvfp4_quantize of the BF16 tensor (two tensors, alternating)")
 
     class Both:
-        def __init__(self, a):
-            self.a = a
+        def __init__(self, a, b):
+            self.a, self.b = a, b
 
         def __call__(self):
             self.a()
-            quant()
+            self.b()
 
-    measure("compact_flow", [Both(c) for c in writer], writer_bytes + quant_bytes,
-            "compact writer + quantize-only per step (bytes: both kernels)")
+    measure("compact_flow", [Both(c, q) for c, q in zip(writer, quants)], writer_bytes + quant_bytes,
+            "compact writer + quantize-only of its output per step (bytes: both kernels)")
     res["compact_flow"]["vs_fused_time"] = None
-    del srcs, compact
+    del srcs, compacts
     torch.cuda.empty_cache()
     wq = W.make("prefill_quantize")
     x = torch.from_numpy(wq.data.view(np.int16)).cuda()
-    pq = torch.empty((wq.rows, wq.width // 2), dtype=torch.uint8, device="cuda")
-    sq = torch.empty((wq.rows, wq.width // 16), dtype=torch.uint8, device="cuda")
-    rc = lib.moe_nvfp4_quantize_scaled(P(x.data_ptr()), wq.rows, wq.width, ctypes.c_float(1.5),
-                                       P(pq.data_ptr()), P(sq.data_ptr()), s)
-    assert rc == 0
+    # two copies of the NVFP4 input, alternating between steps
+    pqs = [torch.empty((wq.rows, wq.width // 2), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    sqs = [torch.empty((wq.rows, wq.width // 16), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    for pq, sq in zip(pqs, sqs):
+        rc = lib.moe_nvfp4_quantize_scaled(P(x.data_ptr()), wq.rows, wq.width, ctypes.c_float(1.5),
+                                           P(pq.data_ptr()), P(sq.data_ptr()), s)
+        assert rc == 0
     del x
     outq = torch.empty((wq.rows, wq.width), dtype=torch.bfloat16, device="cuda")
-    dq = DirectCall(lib.moe_nvfp4_dequantize, (P(pq.data_ptr()), P(sq.data_ptr()), wq.rows,
-                                               wq.width, ctypes.c_float(1.5), P(outq.data_ptr()), s))
-    measure("dequantize", [dq], wq.rows * (wq.width // 2 + wq.width // 16 + 2 * wq.width),
-            "moe_nvfp4_dequantize, global scale 1.5, [65536, 3072]")
+    dqs = [DirectCall(lib.moe_nvfp4_dequantize, (P(pq.data_ptr()), P(sq.data_ptr()), wq.rows, wq.width,
+                                                 ctypes.c_float(1.5), P(outq.data_ptr()), s))
+           for pq, sq in zip(pqs, sqs)]
+    measure("dequantize", dqs, wq.rows * (wq.width // 2 + wq.width // 16 + 2 * wq.width),
+            "moe_nvfp4_dequantize, global scale 1.5, [65536, 3072] (two inputs, alternating)")
     return res
 
 
@@ -894,6 +911,9 @@ def parse(argv=None):
     ap.add_argument("--gemm-case", default=None, metavar="EXPERTS:TOKENS",
                     help="time only the L1 GEMM with the step in its epilogue (top-8 routing, "
                          "H=7168, I=2048) at this size and print its JSON record")
+    ap.add_argument("--extension", default=None, choices=EXTENSION_CASES,
+                    help="time only this extension of the activation step on the ragged "
+                         "workload and print its JSON record")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     return ap.parse_args(argv)
@@ -916,12 +936,29 @@ def main_gemm_case(args):
     print(json.dumps(res), flush=True)
 
 
+def main_extension_case(args):
+    """--extension: one extension of the activation step alone (one JSON record)."""
+    import torch
+    torch.cuda.set_device(0)
+    import moe_swiglu_epilogue_gb300 as M
+    from moe_swiglu_epilogue_gb300 import build, workloads as W
+    build.build()
+    lib = M.load_library()
+    stream = torch.cuda.Stream()
+    peak, _ = measured_peaks()
+    res = extension_measurements(torch, lib, M, W, stream, args.steps, args.warmup, peak,
+                                 only=(args.extension,))
+    print(json.dumps(res), flush=True)
+
+
 def main(argv=None):
     args = parse(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.gemm_case is not None and args.impl == "ours":
         main_gemm_case(args)
+    elif args.extension is not None and args.impl == "ours":
+        main_extension_case(args)
     elif args.impl == "reference":
         main_reference(args)
     else:

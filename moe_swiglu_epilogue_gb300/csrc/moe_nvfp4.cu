@@ -56,7 +56,7 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 2;                 // blocks in flight per lane (fused)
 constexpr int kUnrollQuant = 4;            // blocks in flight per lane (quantize-only)
 constexpr int kMinBlocksFused = 3;         // resident CTAs per SM the register budget targets
-constexpr int kMinBlocksQuant = 4;
+constexpr int kMinBlocksQuant = 3;
 constexpr int kMaxDevices = 64;
 
 // The definition's value: the formula in double precision, rounded once.
@@ -842,9 +842,9 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
                 if (kScaled) v[i] = __fmul_rn(v[i], gs);          // two-level: v = fl(x * gs)
             }
             uint32_t lo, hi;
-            // packed quotient steps pay off only with the scaled values
-            // IEEE reciprocal; the BF16 form keeps fewer registers live
-            const uint32_t code = quantize16_exact<kScaled, kScaled>(v, lo, hi);
+            // packed quotient steps (the register budget of 3 CTAs per SM
+            // holds them and the 4 blocks in flight without spilling)
+            const uint32_t code = quantize16_exact<kScaled, true>(v, lo, hi);
             *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(lo, hi);
             sf[blk] = static_cast<uint8_t>(code);
         }
