@@ -270,7 +270,23 @@ def run_workload(torch, lib, M, W, name: str, steps: int, warmup: int, stream, c
         flush = lambda: scratch.fill_(1)       # evict the small input from L2
     with torch.cuda.stream(stream):
         total_s, per, w0, w1 = time_steps(torch, calls, steps, warmup, stream, flush)
-    return w, total_s, per, w0, w1, (srcs, packed, sf, off)
+    return w, total_s, per, w0, w1, (srcs, packed, sf, off, calls)
+
+
+def launch_percentiles(torch, calls, n: int, stream):
+    """Per-launch durations outside the timed region: each of n launches
+    (inputs alternating as in the timed loop) between its own event pair;
+    p10 / p50 / p90 in microseconds."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            starts[i].record(stream)
+            calls[i % len(calls)]()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    us = np.asarray([a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends)])
+    return [round(float(v), 2) for v in np.percentile(us, [10, 50, 90])]
 
 
 def e2e_measure(torch, lib, w, stream, steps: int, chunks: int = 8):
@@ -771,6 +787,7 @@ def main_ours(args):
                                                   args.warmup, stream)
     sampler.stop()
     clocks = sampler.summary(w0, w1)
+    pcts = launch_percentiles(torch, _keep[4], 100, stream)
     del _keep
     max_s = max_over_ranks(total_s)
     agg = aggregate_throughput(w.algorithmic_bytes(), w.active_rows, args.steps, max_s, world)
@@ -786,6 +803,8 @@ def main_ours(args):
 
     kernel = "nvfp4_quantize_kernel" if w.kind == "quantize" else "swiglu_nvfp4_kernel"
     roof = roofline(w.algorithmic_bytes(), per, peak, peak_src, recorded_traffic(kernel, w.name))
+    roof["launch_us_p10_p50_p90"] = pcts
+    roof["percentiles"] = "100 launches after the timed region, each between its own event pair"
 
     # the extra measurements (other workloads, extensions, the L1 GEMM with
     # 15 GB of weights per process) run in single-GPU runs only
@@ -800,6 +819,7 @@ def main_ours(args):
             ww, tot, per_o, _, _, keep = run_workload(torch, lib, M, W, name, steps,
                                                       min(args.warmup, 20), stream,
                                                       copies=1 if cold else 2, cold_small=cold)
+            pcts_o = None if cold else launch_percentiles(torch, keep[4], 50, stream)
             del keep
             torch.cuda.empty_cache()
             mean_s = statistics.fmean(per_o)
@@ -810,6 +830,8 @@ def main_ours(args):
                 "launch_us_mean": round(mean_s * 1e6, 2),
                 "l2": "flushed before every launch" if cold else "inputs larger than L2",
             }
+            if pcts_o is not None:
+                others[name]["launch_us_p10_p50_p90"] = pcts_o
             if cold:
                 others[name].update(small_config_extras(torch, lib, W, name, stream, per_o))
 

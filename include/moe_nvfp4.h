@@ -196,6 +196,17 @@ MOE_NVFP4_API int moe_swiglu_precise_values(const uint16_t *gu, int64_t rows, in
                                             float clamp_L, float *y, moe_nvfp4_stream_t stream);
 
 /*
+ * Diagnostic: the E4M3 conversion every kernel here takes its scale codes
+ * with (the pages' "FP8 E4M3" scale format: round to nearest even, values
+ * past 448 saturate to 448 = 0x7E), applied to n fp32 values: codes[i] =
+ * E4M3(x[i]). x (fp32 [n]) and codes (uint8 [n]) are DEVICE buffers owned
+ * by the caller. Errors: MOE_NVFP4_ESIZE for n < 0, MOE_NVFP4_ENULL for a
+ * null pointer with n > 0; n == 0 launches nothing.
+ */
+MOE_NVFP4_API int moe_nvfp4_e4m3_codes(const float *x, int64_t n, uint8_t *codes,
+                                       moe_nvfp4_stream_t stream);
+
+/*
  * Diagnostic: as moe_swiglu_nvfp4_quantize, and also adds to the caller's
  * DEVICE counters (uint64 [3], not cleared by the call):
  *   [0] blocks processed, [1] blocks whose scale needed the re-evaluation,
@@ -319,7 +330,7 @@ MOE_NVFP4_API double moe_swiglu_nvfp4_window(float clamp_L);
 /* Static text for a return code. */
 MOE_NVFP4_API const char *moe_nvfp4_strerror(int code);
 
-/* ABI version of this header (incremented on any signature change). */
+/* ABI version of this header (incremented on any signature change or added entry point). */
 MOE_NVFP4_API int moe_nvfp4_abi_version(void);
 
 #ifdef __cplusplus

@@ -17,7 +17,7 @@ import os
 from . import build as _build
 
 __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_values",
-           "moe_swiglu_precise_values", "moe_nvfp4_quantize_scaled",
+           "moe_swiglu_precise_values", "moe_nvfp4_e4m3_codes", "moe_nvfp4_quantize_scaled",
            "moe_swiglu_nvfp4_quantize_ex", "moe_swiglu_bf16", "moe_nvfp4_dequantize",
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
            "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators", "moe_l1_gemm_bf16",
@@ -61,6 +61,8 @@ def load_library():
     lib.moe_swiglu_fast_values.argtypes = [P, I64, I64, F, P, P]
     lib.moe_swiglu_fast_values.restype = ctypes.c_int
     lib.moe_swiglu_precise_values.argtypes = [P, I64, I64, F, P, P]
+    lib.moe_nvfp4_e4m3_codes.argtypes = [P, I64, P, P]
+    lib.moe_nvfp4_e4m3_codes.restype = ctypes.c_int
     lib.moe_swiglu_precise_values.restype = ctypes.c_int
     lib.moe_swiglu_nvfp4_quantize_counted.argtypes = [P, I64, I64, F, P, I32, P, P, P, P]
     lib.moe_swiglu_nvfp4_quantize_counted.restype = ctypes.c_int
@@ -242,6 +244,21 @@ def moe_swiglu_precise_values(gu, clamp_L: float, stream=None):
             ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream))
     _check(rc, "moe_swiglu_precise_values")
     return y
+
+
+def moe_nvfp4_e4m3_codes(x, stream=None):
+    """Diagnostic: the kernels' E4M3 scale conversion of every value of a
+    float32 CUDA tensor (uint8 codes, same shape)."""
+    torch = _torch()
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32):
+        raise TypeError("x must be a float32 CUDA tensor")
+    x = x.contiguous()
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = load_library().moe_nvfp4_e4m3_codes(ctypes.c_void_p(x.data_ptr()), x.numel(),
+                                                 ctypes.c_void_p(codes.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_nvfp4_e4m3_codes")
+    return codes
 
 
 def moe_nvfp4_quantize_scaled(x, global_scale: float, packed=None, sf=None, stream=None):

@@ -793,6 +793,22 @@ swiglu_ex_kernel(const ExArgs X) {
     }
 }
 
+// Diagnostic: the kernels' E4M3 conversion (cvt.rn.satfinite.e4m3x2.f32,
+// the scale step) applied to n fp32 values, two per instruction.
+__global__ void e4m3_codes_kernel(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const int64_t pairs = (n + 1) / 2;
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < pairs;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = 2 * p;
+        const float lo = x[i], hi = (i + 1 < n) ? x[i + 1] : 0.0f;
+        const uint32_t r = e4m3x2_rn_sat(hi, lo);
+        codes[i] = static_cast<uint8_t>(r & 0xFFu);
+        if (i + 1 < n) codes[i + 1] = static_cast<uint8_t>(r >> 8);
+    }
+}
+
 // Diagnostic: the definition-path SwiGLU value of every output element.
 __global__ void swiglu_precise_values_kernel(const uint16_t* __restrict__ gu, int64_t rows,
                                              int64_t I, float L, float* __restrict__ y) {
@@ -1272,6 +1288,17 @@ int moe_swiglu_precise_values(const uint16_t* gu, int64_t rows, int64_t I, float
     return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
 }
 
+int moe_nvfp4_e4m3_codes(const float* x, int64_t n, uint8_t* codes, moe_nvfp4_stream_t stream) {
+    if (n < 0) return MOE_NVFP4_ESIZE;
+    if (n > 0 && (x == nullptr || codes == nullptr)) return MOE_NVFP4_ENULL;
+    if (n == 0) return MOE_NVFP4_OK;
+    DeviceInfo di;
+    int rc;
+    if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    launch(e4m3_codes_kernel, di.sms * 8, reinterpret_cast<cudaStream_t>(stream), x, n, codes);
+    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+}
+
 int moe_swiglu_nvfp4_quantize_counted(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
                                       const int32_t* expert_offsets, int32_t num_experts,
                                       uint8_t* packed, uint8_t* sf, uint64_t* counters,
@@ -1364,6 +1391,6 @@ const char* moe_nvfp4_strerror(int code) {
     }
 }
 
-int moe_nvfp4_abi_version(void) { return 4; }
+int moe_nvfp4_abi_version(void) { return 5; }
 
 }  // extern "C"

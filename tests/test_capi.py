@@ -45,7 +45,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.moe_nvfp4_abi_version() == 4
+    assert lib.moe_nvfp4_abi_version() == 5
     for code in range(0, -10, -1):
         assert lib.moe_nvfp4_strerror(code)
     assert b"unknown" in lib.moe_nvfp4_strerror(-99)
@@ -83,6 +83,14 @@ def test_fused_argument_errors(lib):
     assert f(A32, 4, 40, 7.0, NULL, 0, A16, A16, S) == -2
     assert f(A16, 4, 32, 7.0, NULL, 0, A16, A16, S) == -3
     assert f(A32, 0, 32, 7.0, NULL, 0, A16, A16, S) == 0
+
+
+def test_e4m3_codes_argument_errors(lib):
+    c = lib.moe_nvfp4_e4m3_codes
+    assert c(A16, -1, A16, S) == -4
+    assert c(NULL, 8, A16, S) == -1
+    assert c(A16, 8, NULL, S) == -1
+    assert c(NULL, 0, NULL, S) == 0
 
 
 def test_window(lib):

@@ -9,6 +9,8 @@ exact, and the tests also assert that.
 Small cases run the oracle on every element; full-size cases, in the same
 launch configuration the benchmark times, compare sampled blocks plus every
 block of the first and last active rows."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -127,6 +129,35 @@ def test_quantize_exhaustive_element_map_bit_exact():
     assert set(np.unique(rs)) >= set(range(0, 0x7f))      # every scale code occurs
     assert np.array_equal(gs, rs)
     assert np.array_equal(gp, rp)
+
+
+def test_e4m3_conversion_of_every_nonnegative_finite_fp32():
+    """The scale step's E4M3 conversion (round to nearest even, saturating
+    at 448) on every non-negative finite fp32 bit pattern, 0 .. 0x7F7FFFFF,
+    against the oracle's encoder: in the fused path amax / 6 can be any such
+    value. The oracle runs on all host cores in threads (its C call releases
+    the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
+    end, chunk = 0x7F800000, 1 << 27
+    workers = max(1, os.cpu_count() or 1)
+
+    def encode(bits):
+        return oracle.fp8_e4m3_from_float32_array(bits.view(np.float32))
+
+    with ThreadPoolExecutor(workers) as pool:
+        for start in range(0, end, chunk):
+            n = min(chunk, end - start)
+            x = torch.arange(start, start + n, dtype=torch.int32, device="cuda").view(torch.float32)
+            got = M.moe_nvfp4_e4m3_codes(x).cpu().numpy()
+            bits = np.arange(start, start + n, dtype=np.uint32)
+            parts = np.array_split(bits, 4 * workers)
+            want = np.concatenate(list(pool.map(encode, parts)))
+            if not np.array_equal(got, want):
+                bad = np.flatnonzero(got != want)[:5]
+                raise AssertionError([(hex(int(bits[i])), int(got[i]), int(want[i])) for i in bad])
+    # the ends of the range: +0, the smallest subnormal code, 448, FLT_MAX
+    probe = torch.tensor([0.0, 2.0 ** -9, 448.0, 3.4028235e38], device="cuda")
+    assert M.moe_nvfp4_e4m3_codes(probe).tolist() == [0x00, 0x01, 0x7E, 0x7E]
 
 
 # ---------------------------------------------------------------------------
