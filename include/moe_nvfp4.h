@@ -136,7 +136,9 @@ MOE_NVFP4_API int moe_swiglu_nvfp4_quantize(const uint16_t *gu, int64_t rows, in
  *    the compact writer stores that BF16 tensor [rows, I].
  *  - padded output: input row r of segment e is written to output row
  *    out_offsets[e] + (r - offsets[e]); rows of the output not written keep
- *    their contents; destinations outside [0, out_rows) are skipped.
+ *    their contents; destinations outside [0, out_rows) are skipped. The
+ *    destination ranges of different segments must not overlap (where they
+ *    do, which segment's row lands there is unspecified).
  * All are exact (bit-equal to the definitions, like the entry points above).
  * ------------------------------------------------------------------------- */
 

@@ -56,7 +56,7 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 2;                 // blocks in flight per lane (fused)
 constexpr int kUnrollQuant = 4;            // blocks in flight per lane (quantize-only)
 constexpr int kMinBlocksFused = 3;         // resident CTAs per SM the register budget targets
-constexpr int kMinBlocksQuant = 3;
+constexpr int kMinBlocksQuant = 3;         // quantize-only: 80 registers hold 4 blocks in flight and the packed quotients
 constexpr int kMaxDevices = 64;
 
 // The definition's value: the formula in double precision, rounded once.

@@ -129,6 +129,27 @@ def test_padded_segments_empty_single_row_and_offset_start(I):
         assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
 
 
+@pytest.mark.parametrize("I", [48, 2048])
+def test_padded_destinations_outside_the_output_are_skipped(I):
+    """Segment 0 starts 4 rows before the output and the last one runs past
+    out_rows: those rows are skipped, every other row lands, gaps stay."""
+    offsets = np.array([0, 10, 25, 40], np.int32)
+    out_off = np.array([-4, 12, 30, 45], np.int32)
+    out_rows = 40
+    w = W.fused_normal(rows=40, I=I, seed=13)
+    for gs, compat in ((1.0, False), (1.3, False), (1.0, True)):
+        sent_p = np.full((out_rows, I // 2), 0xA5, np.uint8)
+        sent_s = np.full((out_rows, I // 16), 0x5A, np.uint8)
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(
+            dev(w.data), w.clamp_L, torch.from_numpy(offsets).cuda(), gs, compat,
+            torch.from_numpy(out_off).cuda(), out_rows, torch.from_numpy(sent_p.copy()).cuda(),
+            torch.from_numpy(sent_s.copy()).cuda())
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, w.clamp_L, offsets, out_off, out_rows,
+                                                 gs, compat, packed=sent_p, sf=sent_s)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
+        assert np.all(rp[6:12] == 0xA5) and np.all(rp[27:30] == 0xA5)
+
+
 def test_compact_writer_bit_exact():
     for w in (W.fused_normal(rows=512, I=2048, seed=4), W.prefill_heavy_tail(rows=256, I=3072),
               W.edge_structured(rows=128, I=4096)):

@@ -107,6 +107,12 @@ def test_padded_segments_move_rows_and_leave_gaps(oracle_mod):
                                                 packed=np.full((short, I // 2), 0xA5, np.uint8),
                                                 sf=np.full((short, I // 16), 0x5A, np.uint8))
     assert np.array_equal(p2, p[:short])
+    # destinations before row 0 are skipped too: shifting every destination
+    # 5 rows up drops the first 5 output rows and moves the rest
+    p3, s3 = oracle_mod.swiglu_quantize_nvfp4_ex(w.data, 7.0, w.offsets, out_off - 5, out_rows - 5,
+                                                 packed=np.full((out_rows - 5, I // 2), 0xA5, np.uint8),
+                                                 sf=np.full((out_rows - 5, I // 16), 0x5A, np.uint8))
+    assert np.array_equal(p3, p[5:]) and np.array_equal(s3, s[5:])
 
 
 def test_dequantize_every_nibble_under_every_scale(oracle_mod):
