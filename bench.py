@@ -94,14 +94,42 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_without_comments(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and every run of
+    whitespace collapsed to one space; string and character literals are
+    kept as written."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":                                  # literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources the activation-step kernels are compiled from (the
-    C header holds declarations only)."""
+    """Hash of the code (comments and layout ignored) of the sources the
+    activation-step kernels are compiled from (the C header holds
+    declarations only)."""
     h = hashlib.sha256()
     for rel in ("moe_swiglu_epilogue_gb300/csrc/moe_nvfp4.cu",
                 "moe_swiglu_epilogue_gb300/csrc/nvfp4_device.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            h.update(code_without_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -59,3 +59,17 @@ def test_single_process_needs_no_process_group():
     assert bench.max_over_ranks(3.5) == 3.5
     a = bench.aggregate_throughput(9344, 1, 100, 0.5, 1)
     assert a["gbs"] == pytest.approx(9344 * 100 / 0.5 / 1e9)
+
+
+def test_traffic_record_key_ignores_comments_and_layout():
+    """The ncu traffic record stays valid across comment and whitespace
+    edits of the kernel sources, and not across code edits."""
+    sys.path.insert(0, ROOT)
+    import bench
+    code = 'int f(int a) {  // first\n  /* two\n lines */ return a + 1; }\nconst char* s = "x // y";\n'
+    same = 'int f(int a) { return a + 1; }   /* moved */\nconst char* s = "x // y";'
+    assert bench.code_without_comments(code) == bench.code_without_comments(same)
+    assert bench.code_without_comments(code) != bench.code_without_comments(code.replace("+ 1", "+ 2"))
+    assert bench.code_without_comments(code) != bench.code_without_comments(code.replace("x // y", "x y"))
+    assert "'/'" in bench.code_without_comments("char c = '/'; // slash")
+    assert len(bench.kernel_source_hash()) == 16
