@@ -459,10 +459,10 @@ done:
 // turn each stage in shared memory into the BF16 tile the MMA reads, in the
 // layout a 128-byte-swizzled TMA load would give; e2m1 * e4m3 has at most 6
 // significant bits, so the expansion is exact, and the result equals the
-// BF16 GEMM on the dequantized weights bit for bit. The expansion adds a
-// 32 KB shared-memory write and an 8 KB read to every stage, which makes
-// shared-memory bandwidth, not HBM, the bound: the kernel saves weight
-// memory and HBM traffic, not time, against the BF16-weight kernel.
+// BF16 GEMM on the dequantized weights bit for bit. The latency of the
+// expansion pipeline (nibbles from shared memory, BF16 back into it, then
+// the MMA) sets the pace, not HBM: the kernel saves weight memory and HBM
+// traffic, not time, against the BF16-weight kernel.
 // ---------------------------------------------------------------------------
 
 constexpr int kW4RawStages = 4;                          // x tile + packed weight tile
