@@ -471,6 +471,10 @@ constexpr uint32_t kW4FpBytes = kBN * kBK / 2;           // 8 KB of nibbles per 
 constexpr uint32_t kW4RawBytes = kStageA + kW4FpBytes;   // 24 KB
 constexpr uint32_t kW4ScaleBytes = kBN * 16;             // scales of 4 stages: 16 per row
 constexpr int kW4ScaleSlots = 2;
+// a scale slot serves 4 stages and is reloaded 4 * kW4ScaleSlots stages
+// later, by the producer once the raw stage kW4RawStages back is free: its
+// last reader must be at least that old
+static_assert(kW4RawStages <= 4 * kW4ScaleSlots - 3, "a scale slot outlives its readers");
 constexpr int kW4ConvThreads = 256;
 constexpr int kW4Threads = kGemmThreads + kW4ConvThreads;   // warps 6-13 expand the weights
 
@@ -575,7 +579,7 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                     tma_load_2d(st, &tmX, kb * kBK, static_cast<int>(c.row0), &S.full[s]);
                     tma_load_2d(st + kStageA, &tmQ, kb * (kBK / 2), y_w, &S.full[s]);
                     if (scales)
-                        tma_load_2d(scale_base + ((it >> 2) & 1u) * kW4ScaleBytes, &tmS, (kb >> 2) * 16, y_w,
+                        tma_load_2d(scale_base + ((it >> 2) % kW4ScaleSlots) * kW4ScaleBytes, &tmS, (kb >> 2) * 16, y_w,
                                     &S.full[s]);
                 }
             }
@@ -639,7 +643,7 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                            G.status, 7, G.wait_cycles))
                 break;
             const uint8_t* nib = base + s * kW4RawBytes + kStageA;              // row r at 32 r
-            const uint8_t* sc = scale_base + ((it >> 2) & 1) * kW4ScaleBytes + (it & 3) * 4;   // row r at 16 r
+            const uint8_t* sc = scale_base + ((it >> 2) % kW4ScaleSlots) * kW4ScaleBytes + (it & 3) * 4;   // row r at 16 r
             uint8_t* tile = bconv + j * kStageB;
 #pragma unroll
             for (int i = 0; i < (kBN * 2) / kW4ConvThreads; i++) {
