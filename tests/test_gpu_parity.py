@@ -400,6 +400,65 @@ def _sampled_check(w, gp, gs, n_sample=60000, seed=0):
     assert rep.exact, rep
 
 
+@pytest.mark.parametrize("kind", ["fused", "quantize"])
+def test_inputs_beyond_2_31_elements_sampled(kind):
+    """Maximum-size case: more than 2^31 input elements (4.3 GB), so every
+    index the kernels form must be 64-bit. The input repeats 4099 seeded
+    rows (a prime period: an index that wrapped would land on a row with
+    other content). Rows at both ends, around the repeats and at random are
+    checked against the oracle on their source rows; the fused case also
+    passes an offsets range that leaves two rows at each end untouched."""
+    period, rows = 4099, 65539
+    if kind == "fused":
+        base = W.fused_normal(rows=period, I=16384, seed=21)
+        width_in, nb = 2 * base.width, base.width // 16
+    else:
+        base = W.quantize_normal(rows=period, K=32768, seed=22)
+        width_in, nb = base.width, base.width // 16
+    assert rows * width_in > 2 ** 31
+    src = torch.from_numpy(base.data.view(np.int16)).cuda()
+    x = src.repeat((rows + period - 1) // period, 1)[:rows]
+    del src
+    if kind == "fused":
+        first, last = 2, rows - 2
+        offsets = torch.tensor([first, last], dtype=torch.int32, device="cuda")
+        packed = torch.full((rows, nb * 8), 0xA5, dtype=torch.uint8, device="cuda")
+        sf = torch.full((rows, nb), 0x5A, dtype=torch.uint8, device="cuda")
+        M.moe_swiglu_nvfp4_quantize(x, base.clamp_L, offsets, packed, sf)
+        p2, s2 = M.moe_swiglu_nvfp4_quantize_ex(x, base.clamp_L, global_scale=1.25)   # two-level
+    else:
+        first, last = 0, rows
+        packed, sf = M.moe_nvfp4_quantize(x)
+    torch.cuda.synchronize()
+    del x
+    if kind == "quantize":                                # 4.3 GB of BF16 written back
+        deq = M.moe_nvfp4_dequantize(packed, sf, 1.0)
+    rng = np.random.default_rng(5)
+    check = sorted(set([first, first + 1, period - 1, period, period + 1, 8 * period, rows // 2,
+                        last - 2, last - 1] + list(rng.integers(first, last, 24))))
+    idx = torch.tensor(check, device="cuda")
+    gp, gs = packed[idx].cpu().numpy(), sf[idx].cpu().numpy()
+    for k, r in enumerate(check):
+        src_row = base.data[r % period:r % period + 1]
+        if kind == "fused":
+            rp, rs = oracle.swiglu_quantize_nvfp4(src_row, base.clamp_L)
+        else:
+            rp, rs = oracle.quantize_nvfp4(src_row)
+        assert np.array_equal(gp[k], rp[0]) and np.array_equal(gs[k], rs[0]), r
+    if kind == "fused":                                   # rows outside the range untouched
+        outside = torch.tensor([0, 1, rows - 2, rows - 1], device="cuda")
+        assert bool((packed[outside] == 0xA5).all()) and bool((sf[outside] == 0x5A).all())
+        ep, es = p2[idx].cpu().numpy(), s2[idx].cpu().numpy()
+        for k, r in enumerate(check):
+            rp, rs = oracle.swiglu_quantize_nvfp4_ex(base.data[r % period:r % period + 1], base.clamp_L,
+                                                     global_scale=1.25)
+            assert np.array_equal(ep[k], rp[0]) and np.array_equal(es[k], rs[0]), r
+    else:
+        gd = deq[idx].view(torch.int16).cpu().numpy().view(np.uint16)
+        for k in range(len(check)):
+            assert np.array_equal(gd[k], oracle.dequantize_nvfp4(gp[k:k + 1], gs[k:k + 1], 1.0)[0]), check[k]
+
+
 @pytest.mark.parametrize("name", ["ragged", "prefill", "edge", "prefill_quantize"])
 def test_full_size_workloads_sampled(name):
     w = W.make(name)
