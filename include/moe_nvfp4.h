@@ -40,7 +40,8 @@
  *    cudaStream_t; NULL = the legacy default stream) and the call returns
  *    without waiting for it.
  *  - Input pointers must be 32-byte aligned (256-bit loads); `packed` and
- *    `sf` must be 16-byte aligned.
+ *    `sf` must be 16-byte aligned; expert and output row offsets and the
+ *    GEMMs' status word 4-byte aligned (every entry point below).
  *  - Return 0 on success or a negative MOE_NVFP4_E* code; arguments are
  *    checked on the host before any launch, so a rejected call launches
  *    nothing and leaves the outputs untouched. Faults inside a launched
@@ -203,7 +204,8 @@ MOE_NVFP4_API int moe_swiglu_precise_values(const uint16_t *gu, int64_t rows, in
  * past 448 saturate to 448 = 0x7E), applied to n fp32 values: codes[i] =
  * E4M3(x[i]). x (fp32 [n]) and codes (uint8 [n]) are DEVICE buffers owned
  * by the caller. Errors: MOE_NVFP4_ESIZE for n < 0, MOE_NVFP4_ENULL for a
- * null pointer with n > 0; n == 0 launches nothing.
+ * null pointer with n > 0, MOE_NVFP4_EALIGN for x not 4-byte aligned; n == 0
+ * launches nothing.
  */
 MOE_NVFP4_API int moe_nvfp4_e4m3_codes(const float *x, int64_t n, uint8_t *codes,
                                        moe_nvfp4_stream_t stream);

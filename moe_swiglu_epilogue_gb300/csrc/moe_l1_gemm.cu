@@ -751,6 +751,7 @@ int gemm_device(int& sms) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I, float L,
                 const int32_t* offsets, int32_t E, int mode, uint8_t* packed, uint8_t* sf, void* out,
@@ -768,7 +769,8 @@ int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, 
     if (x == nullptr || w1 == nullptr) return MOE_NVFP4_ENULL;
     if (mode == kOutNvfp4 ? (packed == nullptr || sf == nullptr) : out == nullptr) return MOE_NVFP4_ENULL;
     if (!aligned16(x) || !aligned16(w1) ||
-        (mode == kOutNvfp4 ? (!aligned16(packed) || !aligned16(sf)) : !aligned16(out)))
+        (mode == kOutNvfp4 ? (!aligned16(packed) || !aligned16(sf)) : !aligned16(out)) ||
+        !aligned4(offsets) || !aligned4(status))
         return MOE_NVFP4_EALIGN;
     int sms = 0;
     int rc = gemm_device(sms);
@@ -819,7 +821,8 @@ int launch_gemm_w4(const uint16_t* x, const uint8_t* wq, const uint8_t* ws, int6
     if (x == nullptr || wq == nullptr || ws == nullptr) return MOE_NVFP4_ENULL;
     if (mode == kOutNvfp4 ? (packed == nullptr || sf == nullptr) : acc == nullptr) return MOE_NVFP4_ENULL;
     if (!aligned16(x) || !aligned16(wq) || !aligned16(ws) ||
-        (mode == kOutNvfp4 ? (!aligned16(packed) || !aligned16(sf)) : !aligned16(acc)))
+        (mode == kOutNvfp4 ? (!aligned16(packed) || !aligned16(sf)) : !aligned16(acc)) ||
+        !aligned4(offsets) || !aligned4(status))
         return MOE_NVFP4_EALIGN;
     int sms = 0;
     int rc = gemm_device(sms);

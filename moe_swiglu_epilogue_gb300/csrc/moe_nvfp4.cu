@@ -1188,6 +1188,8 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     if (E < 0 || (E > 0 && offsets == nullptr)) return MOE_NVFP4_EOFFSETS;
     if (out_offsets != nullptr && E == 0) return MOE_NVFP4_EOFFSETS;
     if (out_offsets != nullptr && out_rows < 0) return MOE_NVFP4_ESIZE;
+    if ((E > 0 && !aligned(offsets, 4)) || (out_offsets != nullptr && !aligned(out_offsets, 4)))
+        return MOE_NVFP4_EALIGN;
     if (rows == 0) return MOE_NVFP4_OK;
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
@@ -1222,6 +1224,7 @@ int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int
     const double W = window_for(L);
     if (W < 0.0) return MOE_NVFP4_ECLAMP;
     if (E < 0 || (E > 0 && offsets == nullptr)) return MOE_NVFP4_EOFFSETS;
+    if (E > 0 && !aligned(offsets, 4)) return MOE_NVFP4_EALIGN;
     if (rows == 0) return MOE_NVFP4_OK;
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
@@ -1291,6 +1294,7 @@ int moe_swiglu_precise_values(const uint16_t* gu, int64_t rows, int64_t I, float
 int moe_nvfp4_e4m3_codes(const float* x, int64_t n, uint8_t* codes, moe_nvfp4_stream_t stream) {
     if (n < 0) return MOE_NVFP4_ESIZE;
     if (n > 0 && (x == nullptr || codes == nullptr)) return MOE_NVFP4_ENULL;
+    if (n > 0 && !aligned(x, 4)) return MOE_NVFP4_EALIGN;
     if (n == 0) return MOE_NVFP4_OK;
     DeviceInfo di;
     int rc;

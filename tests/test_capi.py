@@ -83,6 +83,7 @@ def test_fused_argument_errors(lib):
     assert f(A32, 4, 40, 7.0, NULL, 0, A16, A16, S) == -2
     assert f(A16, 4, 32, 7.0, NULL, 0, A16, A16, S) == -3
     assert f(A32, 0, 32, 7.0, NULL, 0, A16, A16, S) == 0
+    assert f(A32, 4, 32, 7.0, A2, 3, A16, A16, S) == -3           # offsets must be 4-byte aligned
 
 
 def test_e4m3_codes_argument_errors(lib):
@@ -90,6 +91,7 @@ def test_e4m3_codes_argument_errors(lib):
     assert c(A16, -1, A16, S) == -4
     assert c(NULL, 8, A16, S) == -1
     assert c(A16, 8, NULL, S) == -1
+    assert c(A2, 8, A16, S) == -3                  # a float pointer must be 4-byte aligned
     assert c(NULL, 0, NULL, S) == 0
 
 
@@ -119,6 +121,9 @@ def test_extension_argument_errors(lib):
     assert ex(A32, 0, 32, 7.0, A16, 2, C.byref(opt), A16, A16, S) == -4
     assert ex(A32, 0, 32, 7.0, NULL, 0, None, A16, A16, S) == 0
     assert ex(A32, 4, 32, 0.0, NULL, 0, None, A16, A16, S) == -5
+    assert ex(A32, 4, 32, 7.0, A2, 2, None, A16, A16, S) == -3     # offsets 4-byte aligned
+    bad_out = FusedOptions(1.0, 0, A2.value, 8)
+    assert ex(A32, 4, 32, 7.0, A16, 2, C.byref(bad_out), A16, A16, S) == -3
     cw = lib.moe_swiglu_bf16
     assert cw(A32, 4, 32, 7.0, NULL, 0, NULL, S) == -1
     assert cw(A32, 4, 32, 7.0, NULL, 0, A2, S) == -3
@@ -146,6 +151,8 @@ def test_gemm_argument_errors(lib):
     assert g(A16, A16, 4, 64, 128, 7.0, A16, 1, NULL, A16, NULL, S) == -1
     assert g(A2, A16, 4, 64, 128, 7.0, A16, 1, A16, A16, NULL, S) == -3
     assert g(A16, A16, 4, 64, 128, 7.0, A16, 1, A16, A2, NULL, S) == -3
+    assert g(A16, A16, 4, 64, 128, 7.0, A2, 1, A16, A16, NULL, S) == -3      # offsets 4-byte aligned
+    assert g(A16, A16, 4, 64, 128, 7.0, A16, 1, A16, A16, A2, S) == -3       # status 4-byte aligned
     assert g(NULL, NULL, 0, 64, 128, 7.0, A16, 1, NULL, NULL, NULL, S) == 0   # nothing to do
     a = lib.moe_l1_gemm_accumulators
     # (x, w1, rows, H, I, offsets, E, acc, status, stream)
