@@ -490,8 +490,8 @@ __device__ __forceinline__ bool outside_window_range(float g, float u, float y, 
     return g < gate_floor || (nonzero && fabsf(y) < 0x1p-100f);
 }
 
-__device__ __forceinline__ uint32_t near_bf16_midpoint(float y, uint32_t tol) {
-    return (((__float_as_uint(y) + (tol - 0x8000u)) & 0xFFFFu) <= 2u * tol) ? 1u : 0u;
+__device__ __forceinline__ uint32_t near_bf16_midpoint(float y, uint32_t c16, uint32_t t16) {
+    return (__float_as_uint(y) * 0x10000u + c16 <= t16) ? 1u : 0u;
 }
 
 __device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool valid, const uint32_t* w,
@@ -509,12 +509,14 @@ __device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool val
         const uint32_t t = static_cast<uint32_t>(ceilf(1.5f * e)) + 2u;
         tol = t < tol ? t : tol;
     }
+    // ((bits + tol - 0x8000) mod 2^16) <= 2 tol, computed in the top half
+    const uint32_t c16 = (tol - 0x8000u) << 16, t16 = ((2u * tol) << 16) | 0xFFFFu;
     uint32_t amb = 0;
 #pragma unroll
     for (int q = 0; q < 8; q++) {
         yb[q] = bf16x2_rn(y[2 * q + 1], y[2 * q]);
-        amb |= (near_bf16_midpoint(y[2 * q], tol) << (2 * q)) |
-               (near_bf16_midpoint(y[2 * q + 1], tol) << (2 * q + 1));
+        amb |= (near_bf16_midpoint(y[2 * q], c16, t16) << (2 * q)) |
+               (near_bf16_midpoint(y[2 * q + 1], c16, t16) << (2 * q + 1));
     }
     // block pre-test for the window's range (gates below the floor, results
     // near underflow); element by element only when it fires
