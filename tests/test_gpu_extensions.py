@@ -150,6 +150,19 @@ def test_padded_destinations_outside_the_output_are_skipped(I):
         assert np.all(rp[6:12] == 0xA5) and np.all(rp[27:30] == 0xA5)
 
 
+@pytest.mark.parametrize("L", [7.3, 0.3, 1234.567])
+def test_extensions_with_a_clamp_not_representable_in_bf16(L):
+    """The extension kernels' fp32-clamp instantiations: two-level, BF16
+    compat (gs = 1 and not) and the compact writer, bit for bit."""
+    w = W.fused_normal(rows=96, I=1024, seed=32, L=L)
+    for gs, compat in ((1.0, False), (1.25, False), (1.0, True), (0.7, True)):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(w.data), L, global_scale=gs, round_to_bf16=compat)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, L, global_scale=gs, round_bf16=compat)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
+    out = M.moe_swiglu_bf16(dev(w.data), L)
+    assert np.array_equal(bits(out), oracle.swiglu_bf16(w.data, L))
+
+
 def test_compact_writer_bit_exact():
     for w in (W.fused_normal(rows=512, I=2048, seed=4), W.prefill_heavy_tail(rows=256, I=3072),
               W.edge_structured(rows=128, I=4096)):

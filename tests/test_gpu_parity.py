@@ -231,6 +231,18 @@ def test_fused_shapes_and_ragged_tails(rows, I):
     check_fused_full(w.data, w.clamp_L, gp, gs, rp, rs)
 
 
+@pytest.mark.parametrize("L", [7.3, 0.3, 1234.567, 1e-3])
+def test_fused_clamp_not_representable_in_bf16(L):
+    """A clamp that is no BF16 value takes the kernels' fp32-clamp
+    instantiation (the BF16x2 clamp is exact only for BF16 values of L);
+    1234.567 is also in the analytic-window regime."""
+    assert float(W.bf16_to_f32(W.bf16_bits(np.array([L], np.float32)))[0]) != float(np.float32(L))
+    w = W.fused_normal(rows=96, I=2048, seed=31, L=L)
+    gp, gs = run_fused(w.data, L)
+    rp, rs = oracle.swiglu_quantize_nvfp4(w.data, L)
+    check_fused_full(w.data, L, gp, gs, rp, rs)
+
+
 def test_zero_rows_is_a_no_op():
     gu = torch.zeros((0, 64), dtype=torch.int16, device="cuda")
     p, s = M.moe_swiglu_nvfp4_quantize(gu, 7.0)
