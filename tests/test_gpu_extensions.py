@@ -161,6 +161,17 @@ def test_extensions_with_a_clamp_not_representable_in_bf16(L):
         assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
     out = M.moe_swiglu_bf16(dev(w.data), L)
     assert np.array_equal(bits(out), oracle.swiglu_bf16(w.data, L))
+    offsets = np.array([3, 40, 41, 90], np.int32)         # padded output, both quantize modes
+    out_off = np.array([0, 48, 64, 128], np.int32)
+    for gs, compat in ((1.25, False), (1.0, True)):
+        sent_p = np.full((128, 512), 0xA5, np.uint8)
+        sent_s = np.full((128, 64), 0x5A, np.uint8)
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(
+            dev(w.data), L, torch.from_numpy(offsets).cuda(), gs, compat, torch.from_numpy(out_off).cuda(), 128,
+            torch.from_numpy(sent_p.copy()).cuda(), torch.from_numpy(sent_s.copy()).cuda())
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, L, offsets, out_off, 128, gs, compat,
+                                                 packed=sent_p, sf=sent_s)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), ("padded", gs, compat)
 
 
 def test_compact_writer_bit_exact():
