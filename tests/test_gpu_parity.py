@@ -241,6 +241,11 @@ def test_fused_clamp_not_representable_in_bf16(L):
     gp, gs = run_fused(w.data, L)
     rp, rs = oracle.swiglu_quantize_nvfp4(w.data, L)
     check_fused_full(w.data, L, gp, gs, rp, rs)
+    counters = torch.zeros(3, dtype=torch.int64, device="cuda")   # the counted instantiation
+    pc, sc = M.moe_swiglu_nvfp4_quantize_counted(dev(w.data), L, counters)
+    torch.cuda.synchronize()
+    assert np.array_equal(pc.cpu().numpy(), gp) and np.array_equal(sc.cpu().numpy(), gs)
+    assert int(counters[0].item()) == 96 * 2048 // 16
 
 
 def test_zero_rows_is_a_no_op():
