@@ -46,6 +46,9 @@ CASES = {
     "tiny": dict(tokens=96, experts=4, topk=2, H=256, I=128, seed=31),
     "ragged_pad": dict(tokens=512, experts=8, topk=2, H=512, I=256, pad_rows=37, seed=32),
     "dense": dict(tokens=200, experts=1, topk=1, H=1024, I=512, seed=33),
+    # the most experts the kernels take (2048): most segments empty, the
+    # others one or a few rows, so nearly every tile is a ragged tail
+    "max_experts": dict(tokens=1024, experts=2048, topk=2, H=256, I=128, seed=34),
 }
 
 
