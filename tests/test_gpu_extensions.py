@@ -150,6 +150,32 @@ def test_padded_destinations_outside_the_output_are_skipped(I):
         assert np.all(rp[6:12] == 0xA5) and np.all(rp[27:30] == 0xA5)
 
 
+@pytest.mark.parametrize("I", [64, 1024])
+def test_padded_many_tiny_segments(I):
+    """3000 segments of 0 to 4 rows (many empty): with I = 64 a 64-block
+    chunk spans 16 rows and several segment ends, so threads step and bisect
+    through the offsets all the time; output segments padded to 4 rows with
+    random gaps."""
+    rng = np.random.default_rng(41)
+    counts = rng.integers(0, 5, 3000)
+    offsets = np.concatenate([[7], 7 + np.cumsum(counts)]).astype(np.int32)
+    rows = int(offsets[-1]) + 5
+    gaps = rng.integers(0, 3, 3000)
+    out_off = np.concatenate([[0], np.cumsum((counts + 3) // 4 * 4 + gaps)]).astype(np.int32)
+    out_rows = int(out_off[-1])
+    w = W.fused_normal(rows=rows, I=I, seed=42)
+    for gs, compat in ((1.0, False), (0.8, True)):
+        sent_p = np.full((out_rows, I // 2), 0xA5, np.uint8)
+        sent_s = np.full((out_rows, I // 16), 0x5A, np.uint8)
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(
+            dev(w.data), w.clamp_L, torch.from_numpy(offsets).cuda(), gs, compat,
+            torch.from_numpy(out_off).cuda(), out_rows, torch.from_numpy(sent_p.copy()).cuda(),
+            torch.from_numpy(sent_s.copy()).cuda())
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, w.clamp_L, offsets, out_off, out_rows,
+                                                 gs, compat, packed=sent_p, sf=sent_s)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
+
+
 @pytest.mark.parametrize("L", [7.3, 0.3, 1234.567])
 def test_extensions_with_a_clamp_not_representable_in_bf16(L):
     """The extension kernels' fp32-clamp instantiations: two-level, BF16
