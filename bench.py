@@ -540,7 +540,8 @@ def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str
             "timing": "mean launch = timed region / launches (back-to-back on one stream)"}
 
 
-EXTENSION_CASES = ("two_level_scale", "bf16_compat", "bf16_compat_scaled", "padded_segments")
+EXTENSION_CASES = ("two_level_scale", "bf16_compat", "bf16_compat_scaled", "padded_segments", "compact_writer",
+                   "dequantize")
 
 
 def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, peak: float,
@@ -591,8 +592,11 @@ def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, pe
                      "frac_of_peak": round(nbytes / mean_s / 1e9 / peak, 4), "bytes": nbytes,
                      "what": note}
 
+    def want(name):
+        return only is None or name in only
+
     for name, opt in opts.items():
-        if only is not None and name not in only:
+        if not want(name):
             continue
         pk, sc = (packed_p, sf_p) if name == "padded_segments" else (packed, sf)
         calls = [DirectCall(lib.moe_swiglu_nvfp4_quantize_ex,
@@ -600,31 +604,35 @@ def extension_measurements(torch, lib, M, W, stream, steps: int, warmup: int, pe
                              ctypes.c_int32(E), ctypes.byref(opt), P(pk.data_ptr()),
                              P(sc.data_ptr()), s)) for x in srcs]
         measure(name, calls, fused_bytes, "moe_swiglu_nvfp4_quantize_ex on the ragged workload")
-    if only is not None:
-        return res
     writer = [DirectCall(lib.moe_swiglu_bf16, (P(x.data_ptr()), rows, I, ctypes.c_float(L),
                                                P(off.data_ptr()), ctypes.c_int32(E),
                                                P(c.data_ptr()), s)) for x, c in zip(srcs, compacts)]
-    measure("compact_writer", writer, writer_bytes, "moe_swiglu_bf16: gate/up -> BF16 [rows, I]")
-    quants = [DirectCall(lib.moe_nvfp4_quantize, (P(c.data_ptr()), rows, I,
-                                                  P(packed.data_ptr()), P(sf.data_ptr()), s))
-              for c in compacts]
-    measure("quantize_of_compact", quants, quant_bytes,
-            "moe_nvfp4_quantize of the BF16 tensor (two tensors, alternating)")
+    if want("compact_writer"):
+        measure("compact_writer", writer, writer_bytes, "moe_swiglu_bf16: gate/up -> BF16 [rows, I]")
+    if only is not None and not want("dequantize"):
+        return res
+    if only is None:                                       # the compact flow: full runs only
+        quants = [DirectCall(lib.moe_nvfp4_quantize, (P(c.data_ptr()), rows, I,
+                                                      P(packed.data_ptr()), P(sf.data_ptr()), s))
+                  for c in compacts]
+        measure("quantize_of_compact", quants, quant_bytes,
+                "moe_nvfp4_quantize of the BF16 tensor (two tensors, alternating)")
 
-    class Both:
-        def __init__(self, a, b):
-            self.a, self.b = a, b
+        class Both:
+            def __init__(self, a, b):
+                self.a, self.b = a, b
 
-        def __call__(self):
-            self.a()
-            self.b()
+            def __call__(self):
+                self.a()
+                self.b()
 
-    measure("compact_flow", [Both(c, q) for c, q in zip(writer, quants)], writer_bytes + quant_bytes,
-            "compact writer + quantize-only of its output per step (bytes: both kernels)")
-    res["compact_flow"]["vs_fused_time"] = None
+        measure("compact_flow", [Both(c, q) for c, q in zip(writer, quants)], writer_bytes + quant_bytes,
+                "compact writer + quantize-only of its output per step (bytes: both kernels)")
+        res["compact_flow"]["vs_fused_time"] = None
     del srcs, compacts
     torch.cuda.empty_cache()
+    if not want("dequantize"):
+        return res
     wq = W.make("prefill_quantize")
     x = torch.from_numpy(wq.data.view(np.int16)).cuda()
     # two copies of the NVFP4 input, alternating between steps
