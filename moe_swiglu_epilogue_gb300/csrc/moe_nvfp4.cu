@@ -554,9 +554,13 @@ __device__ __forceinline__ void resolve_bf16_elements(const FusedArgs& A, int64_
             const uint32_t h = bf16x2_rn(0.0f, swiglu_precise(g, u, A.L));   // low half
             const uint32_t keep = (j & 1) ? 0x0000FFFFu : 0xFFFF0000u;
             const uint32_t put = (j & 1) ? (h << 16) : h;
+            // the word is picked by a one-hot mask: a chain of `t == j / 2`
+            // tests is folded into one indexed store, which moves the whole
+            // array to local memory
+            const uint32_t onehot = 1u << (j >> 1);
 #pragma unroll
             for (int t = 0; t < kN / 2; t++)
-                if (t == (j >> 1)) yb[t] = (yb[t] & keep) | put;
+                if (onehot & (1u << t)) yb[t] = (yb[t] & keep) | put;
         }
     }
 }
@@ -687,8 +691,16 @@ swiglu_ex_kernel(const ExArgs X) {
             const int64_t blk = base + 32 * k + lane;
             if (blk < cta_end) {
                 const uint16_t* p = A.gu + blk * 32;
-                load_stream_32B(p, pol, w[k]);
-                load_stream_32B(p + 16, pol, w[k] + 8);
+                if (kMode == kExCompact) {
+                    // the compact writer (2 output bytes per 4 input bytes)
+                    // streams 8 % faster with plain loads; the quantizing
+                    // modes are faster with the evict-first hint
+                    load_nc_32B(p, w[k]);
+                    load_nc_32B(p + 16, w[k] + 8);
+                } else {
+                    load_stream_32B(p, pol, w[k]);
+                    load_stream_32B(p + 16, pol, w[k] + 8);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; j++) w[k][j] = 0u;

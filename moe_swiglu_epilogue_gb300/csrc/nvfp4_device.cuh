@@ -39,6 +39,14 @@ __device__ __forceinline__ void load_stream_32B(const void* p, uint64_t pol, uin
         : "l"(p), "l"(pol));
 }
 
+// 32 bytes through the read-only path, bypassing L1, default L2 policy.
+__device__ __forceinline__ void load_nc_32B(const void* p, uint32_t* r) {
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]),
+          "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "l"(p));
+}
+
 __device__ __forceinline__ void load_stream_16B(const void* p, uint64_t pol, uint32_t* r) {
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
