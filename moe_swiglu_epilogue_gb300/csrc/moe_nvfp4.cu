@@ -21,7 +21,8 @@
 //     so the active blocks [first, last) are split into equal contiguous
 //     ranges, one per resident CTA, whose warps claim 64-block chunks from a
 //     shared counter; loads are 256-bit, L1-bypassing and marked evict-first
-//     in L2 (the stream is read once), two blocks in flight per lane.
+//     in L2 (the stream is read once; the compact BF16 writer alone streams
+//     faster without the hint), two blocks in flight per lane.
 //   * Each thread owns whole blocks, so the amax needs no shuffles.
 //   * E4M3 scale: cvt.rn.satfinite.e4m3x2.f32 (RNE, saturating at 448);
 //     E2M1 nibbles: the half step is rounded with the exact fp32 trick
