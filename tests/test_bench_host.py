@@ -1,6 +1,7 @@
-"""bench.py's multi-rank host logic on CPU: two gloo ranks, each timing its
-own replica; the reported time is the max over ranks and the throughput
-counts every rank's work (weak scaling)."""
+"""bench.py's host logic on CPU: two gloo ranks, each timing its own
+replica (the reported time is the max over ranks and the throughput counts
+every rank's work: weak scaling); the traffic record's source key; the
+reference arm's JSON line; no output line without a GPU."""
 import os
 import socket
 import sys
@@ -73,3 +74,41 @@ def test_traffic_record_key_ignores_comments_and_layout():
     assert bench.code_without_comments(code) != bench.code_without_comments(code.replace("x // y", "x y"))
     assert "'/'" in bench.code_without_comments("char c = '/'; // slash")
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores and
+    prints one JSON line with the main arm's metric and unit, the `impl`
+    key, its own cpu_baseline and an e2e entry with no device copies."""
+    import json
+    import subprocess
+    sys.path.insert(0, ROOT)
+    import bench
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert "workload" in d["config"]
+
+
+def test_gpu_arm_fails_loudly_without_a_gpu():
+    """With no GPU the bench exits non-zero instead of falling back."""
+    import subprocess
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode != 0
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
