@@ -790,8 +790,10 @@ swiglu_ex_kernel(const ExArgs X) {
                     } else {
 #pragma unroll
                         for (int q = 0; q < 8; q++) {
-                            v[2 * q] = __fmul_rn(bf16_lo(b[q]), X.gs);
-                            v[2 * q + 1] = __fmul_rn(bf16_hi(b[q]), X.gs);
+                            const float2 vv = __fmul2_rn(make_float2(bf16_lo(b[q]), bf16_hi(b[q])),
+                                                         make_float2(X.gs, X.gs));
+                            v[2 * q] = vv.x;
+                            v[2 * q + 1] = vv.y;
                         }
                         code = quantize16_exact<true, true>(v, lo, hi);
                     }
