@@ -317,19 +317,51 @@ def test_dequantize_every_pair_over_global_scales():
             assert np.array_equal(bits(out), oracle.dequantize_nvfp4(packed, sf, gs)), (gs, rows)
 
 
-@pytest.mark.parametrize("name", ["ragged", "prefill"])
-def test_full_size_compat_and_compact_sampled(name):
+@pytest.mark.parametrize("name", ["ragged", "prefill", "edge"])
+def test_full_size_extensions_sampled(name):
+    """Every fused extension at the full workload size, in the launch shape
+    the benchmark times, checked on sampled rows: two-level, BF16 compat
+    with and without a global scale, and the compact writer (the edge
+    workload carries the adversarial blocks: ties, subnormal scales, zeros)."""
     w = W.make(name)
     off = None if w.offsets is None else torch.from_numpy(w.offsets).cuda()
     g = dev(w.data)
-    p, s = M.moe_swiglu_nvfp4_quantize_ex(g, w.clamp_L, off, 1.25, True)
-    out = M.moe_swiglu_bf16(g, w.clamp_L, off)
-    hp, hs, hb = host(p), host(s), bits(out)
     rng = np.random.default_rng(1)
     r0 = 0 if w.offsets is None else int(w.offsets[0])
     r1 = w.rows if w.offsets is None else int(w.offsets[-1])
     rows = rng.integers(r0, r1, 24)
     sub = w.data[rows]
-    rp, rs = oracle.swiglu_quantize_nvfp4_ex(sub, w.clamp_L, global_scale=1.25, round_bf16=True)
-    assert np.array_equal(hs[rows], rs) and np.array_equal(hp[rows], rp)
-    assert np.array_equal(hb[rows], oracle.swiglu_bf16(sub, w.clamp_L))
+    for gs, compat in ((1.25, False), (1.25, True), (1.0, True)):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(g, w.clamp_L, off, gs, compat)
+        hp, hs = host(p), host(s)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(sub, w.clamp_L, global_scale=gs, round_bf16=compat)
+        assert np.array_equal(hs[rows], rs) and np.array_equal(hp[rows], rp), (gs, compat)
+    out = M.moe_swiglu_bf16(g, w.clamp_L, off)
+    assert np.array_equal(bits(out)[rows], oracle.swiglu_bf16(sub, w.clamp_L))
+
+
+def test_full_size_padded_sampled():
+    """Padded output on the full ragged workload, as the benchmark times it
+    (256 expert segments, each padded to 128 output rows): sampled input rows
+    land at their shifted output rows with the oracle's values, and the
+    padding rows after sampled segments keep their sentinel bytes."""
+    w = W.make("ragged")
+    off64 = w.offsets.astype(np.int64)
+    counts = np.diff(off64)
+    padded = (counts + 127) // 128 * 128
+    out_off = np.concatenate([[0], np.cumsum(padded)]).astype(np.int32)
+    out_rows = int(out_off[-1])
+    pk = torch.full((out_rows, w.width // 2), 0xA5, dtype=torch.uint8, device="cuda")
+    sf = torch.full((out_rows, w.width // 16), 0x5A, dtype=torch.uint8, device="cuda")
+    p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(w.data), w.clamp_L, torch.from_numpy(w.offsets).cuda(), 1.0,
+                                         False, torch.from_numpy(out_off).cuda(), out_rows, pk, sf)
+    hp, hs = host(p), host(s)
+    rng = np.random.default_rng(2)
+    rows = rng.integers(int(off64[0]), int(off64[-1]), 24)
+    seg = np.searchsorted(off64, rows, side="right") - 1
+    orow = out_off[seg] + (rows - off64[seg])
+    rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data[rows], w.clamp_L)
+    assert np.array_equal(hs[orow], rs) and np.array_equal(hp[orow], rp)
+    gaps = [int(out_off[e] + counts[e]) for e in np.unique(seg) if padded[e] > counts[e]]
+    assert gaps
+    assert np.all(hp[gaps] == 0xA5) and np.all(hs[gaps] == 0x5A)
