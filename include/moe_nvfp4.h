@@ -320,6 +320,79 @@ MOE_NVFP4_API int moe_l1_gemm_wait_selftest(const uint16_t *x, const uint16_t *w
                                             int32_t *status, int64_t wait_cycles,
                                             moe_nvfp4_stream_t stream);
 
+/*
+ * Diagnostic: the memory traffic of a step with none of its arithmetic, in
+ * the launch shape the step itself takes for the same size (the floor its
+ * kernel can reach on this GPU), or a bare launch, or a read-only sweep:
+ *   MOE_NVFP4_TRAFFIC_FUSED     in BF16 [rows, 2*width]: per 16 outputs, the
+ *                               64 input bytes of moe_swiglu_nvfp4_quantize
+ *                               read, 8 bytes of packed [rows, width/2] and
+ *                               1 byte of sf [rows, width/16] written (the
+ *                               XOR of the words read, so no load is dead)
+ *   MOE_NVFP4_TRAFFIC_QUANTIZE  as above with the 32 input bytes of
+ *                               moe_nvfp4_quantize, in BF16 [rows, width]
+ *   MOE_NVFP4_TRAFFIC_EMPTY     one CTA that does nothing (the cost of a
+ *                               launch); every other argument is ignored
+ *   MOE_NVFP4_TRAFFIC_READ      reads rows * width BF16 values of `in` with
+ *                               the default L2 policy and XORs them into the
+ *                               4 bytes at `packed` (4-byte aligned): a sweep
+ *                               larger than L2 leaves it holding clean lines
+ *                               (a cache flush that creates no write-backs)
+ * Alignment and size rules as moe_swiglu_nvfp4_quantize / moe_nvfp4_quantize;
+ * MOE_NVFP4_EMODE for an unknown kind. No counterpart on the pages: used to
+ * measure how close the kernels run to what their memory access pattern
+ * allows.
+ */
+enum {
+    MOE_NVFP4_TRAFFIC_FUSED = 0,
+    MOE_NVFP4_TRAFFIC_QUANTIZE = 1,
+    MOE_NVFP4_TRAFFIC_EMPTY = 2,
+    MOE_NVFP4_TRAFFIC_READ = 3,
+};
+MOE_NVFP4_API int moe_nvfp4_traffic_floor(const uint16_t *in, int64_t rows, int64_t width,
+                                          int32_t kind, uint8_t *packed, uint8_t *sf,
+                                          moe_nvfp4_stream_t stream);
+
+/*
+ * Checks, on the device, the preconditions the fused entry points place on
+ * their offsets (the expert segments [offsets[e], offsets[e+1]) of
+ * moe_swiglu_nvfp4_quantize and, with padded output, the destination rows
+ * out_offsets[e] + (r - offsets[e]) of moe_swiglu_nvfp4_quantize_ex), which
+ * the kernels themselves do not check: they clamp offsets into the buffers,
+ * so bad offsets never make them access memory out of bounds, but
+ * non-monotone offsets drop or repeat rows, and overlapping destination
+ * ranges make two segments race for the same output rows.
+ *   expert_offsets  DEVICE int32 [num_experts + 1] (required)
+ *   rows            rows of the input
+ *   out_offsets     DEVICE int32 [num_experts + 1] or NULL (then not checked)
+ *   out_rows        rows of the padded output (destination rows are clipped
+ *                   to [0, out_rows) before the overlap test, as the kernel
+ *                   skips the others)
+ *   status          DEVICE int32: the kernel ORs in
+ *                     MOE_NVFP4_CHECK_DECREASING  some offsets[e+1] < offsets[e]
+ *                     MOE_NVFP4_CHECK_OUTSIDE     some offsets[e] outside [0, rows]
+ *                     MOE_NVFP4_CHECK_OVERLAP     two segments' destination rows intersect
+ *                   and never clears a bit: zero it before the call. The
+ *                   kernel never traps; it only writes this word.
+ * Launched on `stream` like the step, so it can be enqueued just before it
+ * (or captured with it in a CUDA graph). The overlap test compares every
+ * pair of segments (num_experts^2 / 2 tests; num_experts <= 16,776,960 with
+ * out_offsets). Errors: MOE_NVFP4_ESIZE for negative sizes or too many
+ * segments, MOE_NVFP4_ENULL, MOE_NVFP4_EALIGN (4-byte alignment).
+ * The specification of the step makes monotone offsets a precondition and
+ * asks for a device-side flag that never traps; this is that check, as a
+ * call of its own rather than a separate build of the library.
+ */
+enum {
+    MOE_NVFP4_CHECK_DECREASING = 1,
+    MOE_NVFP4_CHECK_OUTSIDE = 2,
+    MOE_NVFP4_CHECK_OVERLAP = 4,
+};
+MOE_NVFP4_API int moe_nvfp4_check_offsets(const int32_t *expert_offsets, int32_t num_experts,
+                                          int64_t rows, const int32_t *out_offsets,
+                                          int64_t out_rows, int32_t *status,
+                                          moe_nvfp4_stream_t stream);
+
 /* The relative window the fused kernel uses for a clamp L: a scale or
  * nibble decision whose fast-path input lies within this relative distance
  * of a rounding boundary is redone from the definition's SwiGLU value.

@@ -22,7 +22,12 @@ __all__ = ["moe_nvfp4_quantize", "moe_swiglu_nvfp4_quantize", "moe_swiglu_fast_v
            "moe_swiglu_nvfp4_quantize_counted", "moe_swiglu_nvfp4_window",
            "moe_l1_gemm_swiglu_nvfp4", "moe_l1_gemm_accumulators", "moe_l1_gemm_bf16",
            "moe_l1_gemm_wait_selftest", "moe_l1_gemm_w4_swiglu_nvfp4", "moe_l1_gemm_w4_accumulators",
+           "moe_nvfp4_traffic_floor", "moe_nvfp4_check_offsets", "TRAFFIC_KINDS", "CHECK_BITS",
            "moe_nvfp4_strerror", "MoeNvfp4Error", "library_path", "load_library"]
+
+# include/moe_nvfp4.h: MOE_NVFP4_TRAFFIC_* and MOE_NVFP4_CHECK_*
+TRAFFIC_KINDS = {"fused": 0, "quantize": 1, "empty": 2, "read": 3}
+CHECK_BITS = {"decreasing": 1, "outside": 2, "overlap": 4}
 
 _lib = None
 
@@ -91,6 +96,10 @@ def load_library():
     lib.moe_l1_gemm_wait_selftest.restype = ctypes.c_int
     lib.moe_l1_gemm_bf16.argtypes = [P, P, I64, I64, I64, F, P, I32, I32, P, P, P]
     lib.moe_l1_gemm_bf16.restype = ctypes.c_int
+    lib.moe_nvfp4_traffic_floor.argtypes = [P, I64, I64, I32, P, P, P]
+    lib.moe_nvfp4_traffic_floor.restype = ctypes.c_int
+    lib.moe_nvfp4_check_offsets.argtypes = [P, I32, I64, P, I64, P, P]
+    lib.moe_nvfp4_check_offsets.restype = ctypes.c_int
     lib.moe_nvfp4_abi_version.argtypes = []
     lib.moe_nvfp4_abi_version.restype = ctypes.c_int
     _lib = lib
@@ -500,3 +509,55 @@ def moe_l1_gemm_w4_accumulators(x, w1_packed, w1_sf, expert_offsets, acc=None, s
             _stream_ptr(stream))
     _check(rc, "moe_l1_gemm_w4_accumulators")
     return acc
+
+
+# ---------------------------------------------------------------------------
+# Diagnostics
+# ---------------------------------------------------------------------------
+
+def moe_nvfp4_traffic_floor(kind: str, src=None, width: int = 0, packed=None, sf=None, stream=None):
+    """The memory traffic of a step without its arithmetic, in the step's
+    launch shape: kind "fused" (src BF16 [rows, 2*width]) or "quantize" (src
+    BF16 [rows, width]) writes packed [rows, width/2] and sf [rows, width/16];
+    "empty" launches one idle CTA; "read" sweeps src (read only) and XORs it
+    into packed (uint8 CUDA, >= 4 bytes)."""
+    torch = _torch()
+    code = TRAFFIC_KINDS[kind]
+    z = ctypes.c_void_p(0)
+    dev = src.device if src is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        if kind == "empty":
+            rc = load_library().moe_nvfp4_traffic_floor(z, 0, 0, code, z, z, _stream_ptr(stream))
+        elif kind == "read":
+            n = src.numel() * src.element_size() // 2
+            rc = load_library().moe_nvfp4_traffic_floor(
+                ctypes.c_void_p(src.data_ptr()), n // 16, 16, code, ctypes.c_void_p(packed.data_ptr()), z,
+                _stream_ptr(stream))
+        else:
+            rows = src.shape[0]
+            rc = load_library().moe_nvfp4_traffic_floor(
+                ctypes.c_void_p(src.data_ptr()), rows, int(width), code, ctypes.c_void_p(packed.data_ptr()),
+                ctypes.c_void_p(sf.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_nvfp4_traffic_floor")
+
+
+def moe_nvfp4_check_offsets(expert_offsets, rows: int, out_offsets=None, out_rows: int = 0, status=None,
+                            stream=None):
+    """Checks the offsets' preconditions on the device; returns the int32
+    CUDA status word [1] with CHECK_BITS OR-ed in (0 = none violated). Pass
+    a zeroed `status` to accumulate several checks."""
+    torch = _torch()
+    off_p, E = _offsets_arg(expert_offsets, expert_offsets.device)
+    ooff = ctypes.c_void_p(0)
+    if out_offsets is not None:
+        o_p, E2 = _offsets_arg(out_offsets, expert_offsets.device)
+        if E2 != E:
+            raise ValueError("out_offsets must have as many entries as expert_offsets")
+        ooff = o_p
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=expert_offsets.device)
+    with torch.cuda.device(expert_offsets.device):
+        rc = load_library().moe_nvfp4_check_offsets(off_p, E, int(rows), ooff, int(out_rows),
+                                                    ctypes.c_void_p(status.data_ptr()), _stream_ptr(stream))
+    _check(rc, "moe_nvfp4_check_offsets")
+    return status

@@ -157,9 +157,15 @@ __constant__ float2 kExp2Table[64] = {
     {0x1.f50766p+0f, -0x1.246ebp-26f}, {0x1.fa7c18p+0f, 0x1.9e90d8p-28f},
 };
 
-// e^x for -100 <= x <= 80 as a double-float: x = n ln2/64 + r with
-// |r| <= ln2/128, e^x = 2^(n/64) e^r, e^r by its Taylor series to r^5 (the
-// r^3.. terms in fp32, the rest in double-float).
+// e^x for -100 <= x <= 80 as a double-float, by table-driven range
+// reduction (P. T. P. Tang, "Table-driven implementation of the exponential
+// function in IEEE floating-point arithmetic", ACM TOMS 15(2), 1989):
+// x = n ln2/64 + r with |r| <= ln2/128, e^x = 2^(n/64) e^r, the 64 values
+// 2^(j/64) from a table of fp32 pairs, e^r by its Taylor series to r^5 (the
+// r^3.. terms in fp32, the rest in double-float). The pair arithmetic uses
+// the error-free transformations TwoSum (Knuth, TAOCP vol. 2, 4.2.2),
+// Fast-TwoSum (Dekker 1971) and the FMA form of TwoProduct (Dekker's exact
+// product, with the error term taken by one fma).
 __device__ __forceinline__ DFloat exp_df(float x) {
     const float nf = rintf(__fmul_rn(x, kInvLn2x64));
     const int n = __float2int_rn(nf);
@@ -272,6 +278,8 @@ __device__ __forceinline__ void active_block_range(const int32_t* offsets, int E
 // rounding boundary: every element that could be the true maximum is
 // re-evaluated by the definition (and replaced in y), then the code is taken
 // from the exact amax.
+// The inputs are read again from memory (keeping the loaded words live
+// across the block's arithmetic costs registers on the hot path).
 __device__ __forceinline__ uint32_t scale_by_definition(const uint16_t* blk_in, float L, float W,
                                                         float amax, float* y) {
     const float lim = amax * (1.0f - 2.0f * W);
@@ -315,24 +323,91 @@ __device__ __forceinline__ void fast_swiglu16(const FusedArgs& A, const uint32_t
     }
 }
 
-// Every lane of the warp calls this together (uniform control flow), with
-// `valid` false for lanes past the end of the stream.
-template <bool kCount, bool kValues, bool kBf16Clamp>
-__device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, bool valid,
-                                            const uint32_t* w, Tally& tally) {
+// Elements whose value t = v / d (|v| as given, half step h, residual rr =
+// |t| - h) could lie across a nibble-changing half-step boundary: |rr| +
+// W h > 0.25 (1 - W), with the boundary between half steps k and k+1 among
+// kNibbleChangingBoundaries.
+__device__ __forceinline__ uint32_t near_boundary_elements(const FusedArgs& A, const float* v, float inv) {
+    uint32_t todo = 0;
+    for (int i = 0; i < 16; i++) {
+        const float av = fabsf(v[i]);
+        const float h = fmaf(av, inv, kHalfStepBias) - kHalfStepBias;
+        const float rr = fmaf(av, inv, -h);
+        if (fmaf(A.W, h, fabsf(rr)) > A.near_thr) {
+            const int k = __float2int_rn(2.0f * h) - (rr < 0.0f ? 1 : 0);
+            if (k >= 0 && k < 12 && ((kNibbleChangingBoundaries >> k) & 1u)) todo |= 1u << i;
+        }
+    }
+    return todo;
+}
+
+// Replaces nibble i (0..15) of the stored block at `packed_blk` (its 8
+// packed bytes) with `nib`: clear, then set, by atomics on the 32-bit word
+// holding it, so lanes patching other nibbles of the same word concurrently
+// do not interfere.
+__device__ __forceinline__ void patch_nibble(uint8_t* packed_blk, int i, uint32_t nib) {
+    uint32_t* word = reinterpret_cast<uint32_t*>(packed_blk) + (i >> 3);
+    const int sh = 4 * (i & 7);
+    atomicAnd(word, ~(0xFu << sh));
+    atomicOr(word, nib << sh);
+}
+
+// Re-decides the elements the lanes of a warp left to the definition, after
+// their blocks were stored with the fast nibbles: lane l's `mask` has bit
+// 16 k + i for element i of its k-th block of the chunk, whose scale code is
+// byte k of `codes`. The elements are evaluated 32 at a time, one per lane,
+// whichever lane they belong to (a block near many boundaries, with values
+// on ties, costs its warp one pass, not one pass per element);
+// eval(owner, k, i, code) returns the nibble and patch(owner, k, i, nib,
+// tag) writes it over the stored one (`tag`: the owner's lane value tag0
+// for k = 0, tag1 for k = 1, e.g. where its block was stored). Every lane
+// of the warp calls this together, after the stores it patches.
+template <typename Eval, typename Patch>
+__device__ __forceinline__ void resolve_nibbles_warp(int lane, uint32_t mask, uint32_t codes, Eval eval,
+                                                     Patch patch, int64_t tag0 = 0, int64_t tag1 = 0) {
+    __syncwarp();                                               // the owners' stores before the patches
+    const int cnt = __popc(mask);
+    int pre = cnt;                                              // inclusive prefix over lanes
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(kFullMask, pre, off);
+        if (lane >= off) pre += v;
+    }
+    const int total = __shfl_sync(kFullMask, pre, 31);
+    for (int q0 = 0; q0 < total; q0 += 32) {
+        const int q = min(q0 + lane, total - 1);
+        int owner = 0;                                          // first lane whose prefix exceeds q
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+            const int p = __shfl_sync(kFullMask, pre, owner + step - 1);
+            if (p <= q) owner += step;
+        }
+        const uint32_t omask = __shfl_sync(kFullMask, mask, owner);
+        const int oexcl = __shfl_sync(kFullMask, pre - cnt, owner);
+        const uint32_t ocodes = __shfl_sync(kFullMask, codes, owner);
+        const int64_t otag0 = __shfl_sync(kFullMask, tag0, owner);
+        const int64_t otag1 = __shfl_sync(kFullMask, tag1, owner);
+        if (q0 + lane < total) {
+            uint32_t m = omask;
+            for (int t = q - oexcl; t > 0; t--) m &= m - 1u;    // the (q - oexcl)-th set bit
+            const int bit = __ffs(m) - 1;
+            const int k = bit >> 4, i = bit & 15;
+            patch(owner, k, i, eval(owner, k, i, (ocodes >> (8 * k)) & 0xFFu), k ? otag1 : otag0);
+        }
+    }
+}
+
+// The fused step's fast path for one block of each lane of a warp (blk =
+// the lane's block, valid = inside the lane's range): the block is stored
+// with its fast nibbles; the elements that lie within the window of a
+// nibble-changing boundary are returned (bit i = element i) with the scale
+// code, for resolve_nibbles_warp. Every lane calls this together.
+template <bool kCount, bool kBf16Clamp>
+__device__ __forceinline__ uint32_t fused_block(const FusedArgs& A, int64_t blk, bool valid, const uint32_t* w,
+                                                uint32_t& code_out, Tally& tally) {
     const float L = A.L;
     float y[16];
     fast_swiglu16<kBf16Clamp>(A, w, y);
-    if (kValues) {
-        if (valid) {
-            float4* out = reinterpret_cast<float4*>(A.values + blk * 16);
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-                out[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
-        }
-        return;
-    }
-    const uint16_t* blk_in = A.gu + blk * 32;
 
     // scale: safe when both ends of the window round to the same code (the
     // product by RN(1/6) is within an ulp of amax / 6, inside the window)
@@ -341,7 +416,7 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
     const uint32_t ends = e4m3x2_rn_sat(q * A.Wp1, q * A.Wm1);
     uint32_t code = ends & 0xFFu;
     if (valid && (ends >> 8) != code) {
-        code = scale_by_definition(blk_in, L, A.W, amax, y);
+        code = scale_by_definition(A.gu + blk * 32, L, A.W, amax, y);
         if (kCount) tally.scales++;
     }
 
@@ -353,42 +428,64 @@ __device__ __forceinline__ void fused_block(const FusedArgs& A, int64_t blk, boo
     const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
     float hs[16];
     const float closeness = half_steps16(y, inv, hs);
-    uint32_t lo = e2m1x8(hs), hi = e2m1x8(hs + 8);
-
-    const bool near = valid && closeness > A.near_fast;
-    if (__any_sync(kFullMask, near)) {
-        uint32_t todo = 0;
-        if (near) {
-            for (int i = 0; i < 16; i++) {
-                const float ay = fabsf(y[i]);
-                const float h = fmaf(ay, inv, kHalfStepBias) - kHalfStepBias;
-                const float rr = fmaf(ay, inv, -h);
-                if (fmaf(A.W, h, fabsf(rr)) > A.near_thr) {
-                    // the boundary in question sits between half steps k and k+1
-                    const int k = __float2int_rn(2.0f * h) - (rr < 0.0f ? 1 : 0);
-                    if (k >= 0 && k < 12 && ((kNibbleChangingBoundaries >> k) & 1u)) todo |= 1u << i;
-                }
-            }
-        }
-        // one definition-path SwiGLU per lane per pass, all lanes together
-        while (__any_sync(kFullMask, todo != 0u)) {
-            if (todo != 0u) {
-                const int i = __ffs(todo) - 1;
-                todo &= todo - 1u;
-                float g, u;
-                gate_up_at(blk_in, i, g, u);
-                const uint32_t nib = nibble_by_definition(swiglu_precise(g, u, L), d, code);
-                const int sh = 4 * (i & 7);
-                if (i < 8) lo = (lo & ~(0xFu << sh)) | (nib << sh);
-                else       hi = (hi & ~(0xFu << sh)) | (nib << sh);
-                if (kCount) tally.nibbles++;
-            }
-        }
-    }
     if (valid) {
-        *reinterpret_cast<uint2*>(A.packed + blk * 8) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2*>(A.packed + blk * 8) = make_uint2(e2m1x8(hs), e2m1x8(hs + 8));
         A.sf[blk] = static_cast<uint8_t>(code);
         if (kCount) tally.blocks++;
+    }
+    const bool near = valid && closeness > A.near_fast;
+    uint32_t todo = 0u;
+    if (__any_sync(kFullMask, near) && near) todo = near_boundary_elements(A, y, inv);
+    if (kCount) tally.nibbles += __popc(todo);
+    code_out = code;
+    return todo;
+}
+
+// resolve_nibbles_warp for the plain step's chunk of a warp whose block k
+// of lane l is base + 32 k + l. Out of line: the hot loop keeps none of
+// its registers, and the call runs only when some element of the chunk lies
+// within the window of a boundary.
+__device__ __noinline__ void resolve_chunk(const uint16_t* gu, uint8_t* packed, float L, int64_t base, int lane,
+                                          uint32_t mask, uint32_t codes) {
+    resolve_nibbles_warp(
+        lane, mask, codes,
+        [&](int owner, int k, int i, uint32_t code) {
+            float g, u;
+            gate_up_at(gu + (base + 32 * k + owner) * 32, i, g, u);
+            return nibble_by_definition(swiglu_precise(g, u, L), e4m3_value(code), code);
+        },
+        [&](int owner, int k, int i, uint32_t nib, int64_t) { patch_nibble(packed + (base + 32 * k + owner) * 8, i, nib); });
+}
+
+// The fused step for one chunk of a warp: kUnroll blocks per lane at
+// blk0 + 32 k (k < kUnroll), loaded in w; then one warp-wide re-decision of
+// every element left to the definition in the chunk. Every lane calls this
+// together.
+template <bool kCount, bool kBf16Clamp>
+__device__ __forceinline__ void fused_chunk(const FusedArgs& A, int64_t blk0, int64_t end, int lane,
+                                            const uint32_t (*w)[16], Tally& tally) {
+    static_assert(kUnroll * 16 <= 32 && kUnroll * 8 <= 32, "element bits and codes fit a word");
+    uint32_t mask = 0, codes = 0;
+#pragma unroll
+    for (int k = 0; k < kUnroll; k++) {
+        uint32_t code;
+        mask |= fused_block<kCount, kBf16Clamp>(A, blk0 + 32 * k, blk0 + 32 * k < end, w[k], code, tally)
+                << (16 * k);
+        codes |= code << (8 * k);
+    }
+    if (__any_sync(kFullMask, mask != 0u)) resolve_chunk(A.gu, A.packed, A.L, blk0 - lane, lane, mask, codes);
+}
+
+// The diagnostic variant: the fast fp32 values of one block, in output
+// column order.
+template <bool kBf16Clamp>
+__device__ __forceinline__ void fast_values_block(const FusedArgs& A, int64_t blk, bool valid, const uint32_t* w) {
+    float y[16];
+    fast_swiglu16<kBf16Clamp>(A, w, y);
+    if (valid) {
+        float4* out = reinterpret_cast<float4*>(A.values + blk * 16);
+#pragma unroll
+        for (int k = 0; k < 4; k++) out[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
     }
 }
 
@@ -403,8 +500,8 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
     const int lane = threadIdx.x & 31;
     // Each CTA owns an equal contiguous range of blocks; its warps claim
     // chunks of 32 * kUnroll blocks from a shared counter, so a warp held up
-    // by a rare exact re-evaluation (or slow memory) takes fewer chunks and
-    // the CTA's other warps absorb the delay.
+    // by exact re-evaluations (or slow memory) takes fewer chunks and the
+    // CTA's other warps absorb the delay.
     constexpr int64_t kChunk = 32 * kUnroll;
     const int64_t total = b1 - b0;
     int64_t per_cta = (total + gridDim.x - 1) / gridDim.x;
@@ -434,10 +531,12 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
                 for (int j = 0; j < 16; j++) w[k][j] = 0u;
             }
         }
+        if (kValues) {
 #pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + 32 * k + lane;
-            fused_block<kCount, kValues, kBf16Clamp>(A, blk, blk < cta_end, w[k], tally);
+            for (int k = 0; k < kUnroll; k++)
+                fast_values_block<kBf16Clamp>(A, base + 32 * k + lane, base + 32 * k + lane < cta_end, w[k]);
+        } else {
+            fused_chunk<kCount, kBf16Clamp>(A, base + lane, cta_end, lane, w, tally);
         }
     }
     if (kCount) {
@@ -445,6 +544,39 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
         if (tally.scales) atomicAdd(A.counters + 1, tally.scales);
         if (tally.nibbles) atomicAdd(A.counters + 2, tally.nibbles);
     }
+}
+
+// Small problems, where every block fits in one wave of resident threads at
+// one block per thread: thread t of the grid takes block first + t, so every
+// warp has work, every lane's loads are in flight before any arithmetic, and
+// there is no chunk loop (the persistent shape above would give a few CTAs
+// several chunks each and leave most warps idle). CTAs of whole warps;
+// blockDim.x is chosen on the host.
+template <bool kBf16Clamp>
+__global__ void __launch_bounds__(kThreads)
+swiglu_nvfp4_small_kernel(const FusedArgs A) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    int64_t b0, b1;
+    active_block_range(A.offsets, A.E, A.rows, A.bpr, b0, b1);
+    const int64_t blk = b0 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const bool valid = blk < b1;
+    if (__all_sync(kFullMask, !valid)) return;             // warp-uniform
+    uint32_t w[16];
+    if (valid) {
+        const uint64_t pol = l2_evict_first_policy();
+        const uint16_t* p = A.gu + blk * 32;
+        load_stream_32B(p, pol, w);
+        load_stream_32B(p + 16, pol, w + 8);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; j++) w[j] = 0u;
+    }
+    Tally tally;
+    uint32_t code;
+    const uint32_t todo = fused_block<false, kBf16Clamp>(A, blk, valid, w, code, tally);
+    if (__any_sync(kFullMask, todo != 0u))
+        resolve_chunk(A.gu, A.packed, A.L, blk - (threadIdx.x & 31), threadIdx.x & 31, todo, code);
 }
 
 // ---------------------------------------------------------------------------
@@ -884,6 +1016,30 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
     }
 }
 
+// Quantize-only for small problems: one block per thread (as
+// swiglu_nvfp4_small_kernel), the load issued first.
+template <bool kScaled>
+__global__ void __launch_bounds__(kThreads)
+nvfp4_quantize_small_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
+                            uint8_t* __restrict__ packed, uint8_t* __restrict__ sf) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (blk >= nblk) return;
+    uint32_t w[8];
+    load_stream_32B(x + blk * 16, l2_evict_first_policy(), w);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        v[i] = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+        if (kScaled) v[i] = __fmul_rn(v[i], gs);
+    }
+    uint32_t lo, hi;
+    const uint32_t code = quantize16_exact<kScaled, true>(v, lo, hi);
+    *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(lo, hi);
+    sf[blk] = static_cast<uint8_t>(code);
+}
+
 // ---------------------------------------------------------------------------
 // Dequantization: NVFP4 -> BF16, value = e2m1 * e4m3 / gs
 // ---------------------------------------------------------------------------
@@ -971,6 +1127,194 @@ nvfp4_dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __res
 }
 
 // ---------------------------------------------------------------------------
+// Diagnostics: the memory system's limit for this step's traffic, and the
+// preconditions on expert offsets
+// ---------------------------------------------------------------------------
+
+template <int n>
+__device__ __forceinline__ uint32_t xor_fold(const uint32_t* w) {
+    uint32_t r = w[0];
+#pragma unroll
+    for (int i = 1; i < n; i++) r ^= w[i];
+    return r;
+}
+
+// The loads and stores of one block with none of the arithmetic: the folded
+// input words stand in for the 8 packed bytes and the scale byte, so no
+// load is dead.
+template <int kInWords>
+__device__ __forceinline__ void floor_store(const uint32_t* w, int64_t blk, uint8_t* packed, uint8_t* sf) {
+    const uint32_t a = xor_fold<kInWords / 2>(w), b = xor_fold<kInWords / 2>(w + kInWords / 2);
+    *reinterpret_cast<uint2*>(packed + blk * 8) = make_uint2(a, b);
+    sf[blk] = static_cast<uint8_t>(a ^ b);
+}
+
+template <int kInWords>
+__device__ __forceinline__ void floor_load(const uint32_t* in, int64_t blk, uint64_t pol, uint32_t* w) {
+    load_stream_32B(in + blk * kInWords, pol, w);
+    if (kInWords == 16) load_stream_32B(in + blk * kInWords + 8, pol, w + 8);
+}
+
+// The fused step's traffic (64 input bytes per block) in its persistent
+// shape: CTA ranges, 64-block chunks claimed from a shared counter, two
+// blocks in flight per lane.
+__global__ void __launch_bounds__(kThreads, kMinBlocksFused)
+fused_traffic_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8_t* sf) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const uint64_t pol = l2_evict_first_policy();
+    const int lane = threadIdx.x & 31;
+    constexpr int64_t kChunk = 32 * kUnroll;
+    int64_t per_cta = (nblk + gridDim.x - 1) / gridDim.x;
+    per_cta = (per_cta + kChunk - 1) / kChunk * kChunk;
+    const int64_t cta_begin = static_cast<int64_t>(blockIdx.x) * per_cta;
+    const int64_t cta_end = cta_begin + per_cta < nblk ? cta_begin + per_cta : nblk;
+    __shared__ int next_chunk;
+    if (threadIdx.x == 0) next_chunk = 0;
+    __syncthreads();
+    for (;;) {
+        int c = 0;
+        if (lane == 0) c = atomicAdd(&next_chunk, 1);
+        c = __shfl_sync(kFullMask, c, 0);
+        const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
+        if (base >= cta_end) break;
+        uint32_t w[kUnroll][16];
+#pragma unroll
+        for (int k = 0; k < kUnroll; k++)
+            if (base + 32 * k + lane < cta_end) floor_load<16>(in, base + 32 * k + lane, pol, w[k]);
+#pragma unroll
+        for (int k = 0; k < kUnroll; k++)
+            if (base + 32 * k + lane < cta_end) floor_store<16>(w[k], base + 32 * k + lane, packed, sf);
+    }
+}
+
+// The quantize-only step's traffic (32 input bytes per block) in its
+// persistent shape: grid-stride, four blocks in flight per lane.
+__global__ void __launch_bounds__(kThreads, kMinBlocksQuant)
+quantize_traffic_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8_t* sf) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const uint64_t pol = l2_evict_first_policy();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnrollQuant;
+    for (int64_t base = warp * 32 * kUnrollQuant; base < nblk; base += step) {
+        uint32_t w[kUnrollQuant][8];
+#pragma unroll
+        for (int k = 0; k < kUnrollQuant; k++)
+            if (base + 32 * k + lane < nblk) floor_load<8>(in, base + 32 * k + lane, pol, w[k]);
+#pragma unroll
+        for (int k = 0; k < kUnrollQuant; k++)
+            if (base + 32 * k + lane < nblk) floor_store<8>(w[k], base + 32 * k + lane, packed, sf);
+    }
+}
+
+// Either step's traffic in the small-problem shape: one block per thread.
+template <int kInWords>
+__global__ void __launch_bounds__(kThreads)
+traffic_small_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8_t* sf) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (blk >= nblk) return;
+    uint32_t w[kInWords];
+    floor_load<kInWords>(in, blk, l2_evict_first_policy(), w);
+    floor_store<kInWords>(w, blk, packed, sf);
+}
+
+// A launch and nothing else.
+__global__ void empty_kernel() {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+}
+
+// Reads n32 32-byte pieces with the default L2 policy (four in flight per
+// thread) and XORs them into *sink, one atomic per CTA: a read-only sweep
+// that replaces the L2's contents with clean lines.
+__global__ void __launch_bounds__(kThreads)
+read_sweep_kernel(const uint32_t* in, int64_t n32, uint32_t* sink) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    uint32_t acc = 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n32; i += 4 * stride) {
+        uint32_t w[4][8];
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (i + k * stride < n32) load_nc_32B(in + (i + k * stride) * 8, w[k]);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (i + k * stride < n32) acc ^= xor_fold<8>(w[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(kFullMask, acc, o);
+    __shared__ uint32_t warp_acc[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_acc[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t a = 0;
+        for (int k = 0; k < kThreads / 32; k++) a ^= warp_acc[k];
+        atomicXor(sink, a);
+    }
+}
+
+// Preconditions of the expert offsets, checked on the device (the offsets
+// live there): bit MOE_NVFP4_CHECK_DECREASING when offsets[e+1] <
+// offsets[e], MOE_NVFP4_CHECK_OUTSIDE when an offset lies outside [0, rows],
+// and with padded output MOE_NVFP4_CHECK_OVERLAP when the destination rows
+// of two segments (each clipped to [0, out_rows)) intersect. Bits are OR-ed
+// into *status; nothing traps. Grid: x over offsets (and segments i), y over
+// tiles of segments j compared with i (only tiles at or past i's tile).
+constexpr int kCheckTile = 256;
+
+__device__ __forceinline__ void dest_range(const int32_t* offsets, const int32_t* out_offsets, int64_t out_rows,
+                                           int64_t e, int64_t& lo, int64_t& hi) {
+    const int64_t n = static_cast<int64_t>(__ldg(offsets + e + 1)) - __ldg(offsets + e);
+    lo = __ldg(out_offsets + e);
+    hi = lo + (n > 0 ? n : 0);
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > out_rows ? out_rows : hi;
+}
+
+__global__ void __launch_bounds__(kCheckTile)
+check_offsets_kernel(const int32_t* offsets, int E, int64_t rows, const int32_t* out_offsets,
+                     int64_t out_rows, int32_t* status) {
+    wait_for_preceding_grid();
+    allow_next_grid_launch();
+    int bits = 0;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kCheckTile + threadIdx.x;
+    if (blockIdx.y == 0 && i <= E) {
+        const int64_t o = __ldg(offsets + i);
+        if (o < 0 || o > rows) bits |= MOE_NVFP4_CHECK_OUTSIDE;
+        if (i < E && __ldg(offsets + i + 1) < o) bits |= MOE_NVFP4_CHECK_DECREASING;
+    }
+    if (out_offsets != nullptr && blockIdx.y >= blockIdx.x) {
+        __shared__ int64_t lo_s[kCheckTile], hi_s[kCheckTile];
+        const int64_t j = static_cast<int64_t>(blockIdx.y) * kCheckTile + threadIdx.x;
+        int64_t lo = 0, hi = 0;
+        if (j < E) dest_range(offsets, out_offsets, out_rows, j, lo, hi);
+        lo_s[threadIdx.x] = lo;
+        hi_s[threadIdx.x] = hi;
+        __syncthreads();
+        if (i < E) {
+            int64_t ilo, ihi;
+            dest_range(offsets, out_offsets, out_rows, i, ilo, ihi);
+            if (ilo < ihi) {
+                for (int t = 0; t < kCheckTile; t++) {
+                    const int64_t jj = static_cast<int64_t>(blockIdx.y) * kCheckTile + t;
+                    if (jj > i && jj < E && lo_s[t] < hi_s[t] &&
+                        (ilo > lo_s[t] ? ilo : lo_s[t]) < (ihi < hi_s[t] ? ihi : hi_s[t])) {
+                        bits |= MOE_NVFP4_CHECK_OVERLAP;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    if (bits != 0) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -981,6 +1325,7 @@ struct DeviceInfo {
     int occ_ex[2][7] = {};          // [bf16 clamp][ExMode, then padded kExQuantize, kExCompat, kExCompatUnit]
     int occ_quant[2] = {0, 0};                  // [scaled]
     int occ_dequant = 0;
+    int occ_traffic[2] = {0, 0};                // [fused, quantize] traffic-floor kernels
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -1028,7 +1373,11 @@ int device_info(DeviceInfo& out) {
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &di.occ_quant[1], nvfp4_quantize_kernel<true>, kThreads, 0) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &di.occ_dequant, nvfp4_dequantize_kernel<kDivMarkstein>, kThreads, 0) != cudaSuccess)
+                &di.occ_dequant, nvfp4_dequantize_kernel<kDivMarkstein>, kThreads, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &di.occ_traffic[0], fused_traffic_kernel, kThreads, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &di.occ_traffic[1], quantize_traffic_kernel, kThreads, 0) != cudaSuccess)
             return MOE_NVFP4_ELAUNCH;
         di.ready = true;
     }
@@ -1042,6 +1391,20 @@ int grid_for(int64_t nblk, int sms, int occ, int unroll = kUnroll) {
     const int64_t want = (nblk + per_cta - 1) / per_cta;
     const int64_t cap = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+// Small-problem shape: when every block fits in one wave of the resident
+// threads at one block per thread, one block per thread in CTAs of
+// kSmallThreads (small CTAs spread the few blocks over every SM).
+constexpr int kSmallThreads = 128;
+
+bool small_problem(int64_t nblk, int sms, int occ) {
+    return nblk <= static_cast<int64_t>(sms) * (occ > 0 ? occ : 1) * kThreads;
+}
+
+int small_grid(int64_t nblk) {
+    const int64_t g = (nblk + kSmallThreads - 1) / kSmallThreads;
+    return static_cast<int>(g < 1 ? 1 : g);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -1122,10 +1485,11 @@ int64_t bf16_bits_of(float L) {
 // overlaps the tail of the preceding one (each kernel above waits for it
 // before touching memory).
 template <typename... KArgs, typename... Args>
-cudaError_t launch(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args&&... args) {
+cudaError_t launch_shaped(void (*kernel)(KArgs...), dim3 grid, int threads, cudaStream_t stream,
+                          Args&&... args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1136,17 +1500,26 @@ cudaError_t launch(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), int grid, cudaStream_t stream, Args&&... args) {
+    return launch_shaped(kernel, dim3(static_cast<unsigned>(grid)), kThreads, stream,
+                         std::forward<Args>(args)...);
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH; }
+
 template <bool kBf16Clamp>
-void launch_fused_kernel(const FusedArgs& A, int64_t nblk, const DeviceInfo& di, bool counted,
-                         bool values, cudaStream_t stream) {
+cudaError_t launch_fused_kernel(const FusedArgs& A, int64_t nblk, const DeviceInfo& di, bool counted,
+                                bool values, cudaStream_t stream) {
     const int* occ = di.occ[kBf16Clamp ? 1 : 0];
-    if (values) {
-        launch(swiglu_nvfp4_kernel<false, true, kBf16Clamp>, grid_for(nblk, di.sms, occ[2]), stream, A);
-    } else if (counted) {
-        launch(swiglu_nvfp4_kernel<true, false, kBf16Clamp>, grid_for(nblk, di.sms, occ[1]), stream, A);
-    } else {
-        launch(swiglu_nvfp4_kernel<false, false, kBf16Clamp>, grid_for(nblk, di.sms, occ[0]), stream, A);
-    }
+    if (values)
+        return launch(swiglu_nvfp4_kernel<false, true, kBf16Clamp>, grid_for(nblk, di.sms, occ[2]), stream, A);
+    if (counted)
+        return launch(swiglu_nvfp4_kernel<true, false, kBf16Clamp>, grid_for(nblk, di.sms, occ[1]), stream, A);
+    if (small_problem(nblk, di.sms, occ[0]))
+        return launch_shaped(swiglu_nvfp4_small_kernel<kBf16Clamp>, dim3(small_grid(nblk)), kSmallThreads,
+                             stream, A);
+    return launch(swiglu_nvfp4_kernel<false, false, kBf16Clamp>, grid_for(nblk, di.sms, occ[0]), stream, A);
 }
 
 bool valid_scale(float gs) { return std::isfinite(gs) && gs > 0.0f; }
@@ -1172,24 +1545,23 @@ FusedArgs fused_args(const uint16_t* gu, int64_t rows, int64_t I, float L, doubl
 }
 
 template <bool kBf16Clamp>
-void launch_ex_kernel(const ExArgs& X, int mode, int64_t nblk, const DeviceInfo& di,
-                      cudaStream_t stream) {
+cudaError_t launch_ex_kernel(const ExArgs& X, int mode, int64_t nblk, const DeviceInfo& di,
+                             cudaStream_t stream) {
     const int* occ = di.occ_ex[kBf16Clamp ? 1 : 0];
     const bool padded = X.out_offsets != nullptr && X.f.offsets != nullptr;
     if (mode == kExQuantize && padded)
-        launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[4]), stream, X);
-    else if (mode == kExQuantize)
-        launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[0]), stream, X);
-    else if (mode == kExCompat && X.gs == 1.0f && padded)
-        launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[6]), stream, X);
-    else if (mode == kExCompat && X.gs == 1.0f)
-        launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[3]), stream, X);
-    else if (mode == kExCompat && padded)
-        launch(swiglu_ex_kernel<kExCompat, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[5]), stream, X);
-    else if (mode == kExCompat)
-        launch(swiglu_ex_kernel<kExCompat, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[1]), stream, X);
-    else
-        launch(swiglu_ex_kernel<kExCompact, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[2]), stream, X);
+        return launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[4]), stream, X);
+    if (mode == kExQuantize)
+        return launch(swiglu_ex_kernel<kExQuantize, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[0]), stream, X);
+    if (mode == kExCompat && X.gs == 1.0f && padded)
+        return launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[6]), stream, X);
+    if (mode == kExCompat && X.gs == 1.0f)
+        return launch(swiglu_ex_kernel<kExCompatUnit, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[3]), stream, X);
+    if (mode == kExCompat && padded)
+        return launch(swiglu_ex_kernel<kExCompat, kBf16Clamp, true>, grid_for(nblk, di.sms, occ[5]), stream, X);
+    if (mode == kExCompat)
+        return launch(swiglu_ex_kernel<kExCompat, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[1]), stream, X);
+    return launch(swiglu_ex_kernel<kExCompact, kBf16Clamp, false>, grid_for(nblk, di.sms, occ[2]), stream, X);
 }
 
 int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_t* offsets,
@@ -1226,9 +1598,8 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     // the per-gate silu bound was measured with gates clamped at 100
     X.mid_tol_per_block = L <= 100.0f ? 1 : 0;
     const int64_t nblk = rows * (I / 16);
-    if (bf16_bits_of(L) >= 0) launch_ex_kernel<true>(X, mode, nblk, di, stream);
-    else launch_ex_kernel<false>(X, mode, nblk, di, stream);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+    return launch_status(bf16_bits_of(L) >= 0 ? launch_ex_kernel<true>(X, mode, nblk, di, stream)
+                                              : launch_ex_kernel<false>(X, mode, nblk, di, stream));
 }
 
 int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_t* offsets,
@@ -1260,9 +1631,21 @@ int launch_fused(const uint16_t* gu, int64_t rows, int64_t I, float L, const int
     A.packed = packed; A.sf = sf;
     A.counters = reinterpret_cast<unsigned long long*>(counters); A.values = values;
     const int64_t nblk = rows * (I / 16);
-    if (lb >= 0) launch_fused_kernel<true>(A, nblk, di, counters != nullptr, values != nullptr, stream);
-    else launch_fused_kernel<false>(A, nblk, di, counters != nullptr, values != nullptr, stream);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+    return launch_status(
+        lb >= 0 ? launch_fused_kernel<true>(A, nblk, di, counters != nullptr, values != nullptr, stream)
+                : launch_fused_kernel<false>(A, nblk, di, counters != nullptr, values != nullptr, stream));
+}
+
+// The quantize-only kernels in the shape for nblk blocks.
+template <bool kScaled>
+cudaError_t launch_quantize(const uint16_t* x, int64_t nblk, float gs, uint8_t* packed, uint8_t* sf,
+                            const DeviceInfo& di, cudaStream_t stream) {
+    const int occ = di.occ_quant[kScaled ? 1 : 0];
+    if (small_problem(nblk, di.sms, occ))
+        return launch_shaped(nvfp4_quantize_small_kernel<kScaled>, dim3(small_grid(nblk)), kSmallThreads,
+                             stream, x, nblk, gs, packed, sf);
+    return launch(nvfp4_quantize_kernel<kScaled>, grid_for(nblk, di.sms, occ, kUnrollQuant), stream, x, nblk,
+                  gs, packed, sf);
 }
 
 }  // namespace
@@ -1276,9 +1659,8 @@ int moe_nvfp4_quantize(const uint16_t* x, int64_t rows, int64_t K, uint8_t* pack
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     const int64_t nblk = rows * (K / 16);
-    launch(nvfp4_quantize_kernel<false>, grid_for(nblk, di.sms, di.occ_quant[0], kUnrollQuant),
-           reinterpret_cast<cudaStream_t>(stream), x, nblk, 1.0f, packed, sf);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+    return launch_status(launch_quantize<false>(x, nblk, 1.0f, packed, sf, di,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_swiglu_nvfp4_quantize(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
@@ -1303,9 +1685,8 @@ int moe_swiglu_precise_values(const uint16_t* gu, int64_t rows, int64_t I, float
     if (rows == 0) return MOE_NVFP4_OK;
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
-    launch(swiglu_precise_values_kernel, di.sms * 8, reinterpret_cast<cudaStream_t>(stream), gu, rows,
-           I, clamp_L, y);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+    return launch_status(launch(swiglu_precise_values_kernel, di.sms * 8, reinterpret_cast<cudaStream_t>(stream),
+                                gu, rows, I, clamp_L, y));
 }
 
 int moe_nvfp4_e4m3_codes(const float* x, int64_t n, uint8_t* codes, moe_nvfp4_stream_t stream) {
@@ -1316,8 +1697,8 @@ int moe_nvfp4_e4m3_codes(const float* x, int64_t n, uint8_t* codes, moe_nvfp4_st
     DeviceInfo di;
     int rc;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
-    launch(e4m3_codes_kernel, di.sms * 8, reinterpret_cast<cudaStream_t>(stream), x, n, codes);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+    return launch_status(launch(e4m3_codes_kernel, di.sms * 8, reinterpret_cast<cudaStream_t>(stream), x, n,
+                                codes));
 }
 
 int moe_swiglu_nvfp4_quantize_counted(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
@@ -1339,9 +1720,8 @@ int moe_nvfp4_quantize_scaled(const uint16_t* x, int64_t rows, int64_t K, float 
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     const int64_t nblk = rows * (K / 16);
-    launch(nvfp4_quantize_kernel<true>, grid_for(nblk, di.sms, di.occ_quant[1], kUnrollQuant),
-           reinterpret_cast<cudaStream_t>(stream), x, nblk, global_scale, packed, sf);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+    return launch_status(launch_quantize<true>(x, nblk, global_scale, packed, sf, di,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_swiglu_nvfp4_quantize_ex(const uint16_t* gu, int64_t rows, int64_t I, float clamp_L,
@@ -1383,15 +1763,73 @@ int moe_nvfp4_dequantize(const uint8_t* packed, const uint8_t* sf, int64_t rows,
     // every quotient, residual and RN(1/gs) is a normal fp32 number
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (global_scale == 1.0f)
-        launch(nvfp4_dequantize_kernel<kDivNone>, static_cast<int>(grid), st, packed, sf, nblk,
-               global_scale, out);
-    else if (global_scale >= 0x1p-90f && global_scale <= 0x1p90f)
-        launch(nvfp4_dequantize_kernel<kDivMarkstein>, static_cast<int>(grid), st, packed, sf,
-               nblk, global_scale, out);
-    else
-        launch(nvfp4_dequantize_kernel<kDivIeee>, static_cast<int>(grid), st, packed, sf, nblk,
-               global_scale, out);
-    return cudaGetLastError() == cudaSuccess ? MOE_NVFP4_OK : MOE_NVFP4_ELAUNCH;
+        return launch_status(launch(nvfp4_dequantize_kernel<kDivNone>, static_cast<int>(grid), st, packed,
+                                    sf, nblk, global_scale, out));
+    if (global_scale >= 0x1p-90f && global_scale <= 0x1p90f)
+        return launch_status(launch(nvfp4_dequantize_kernel<kDivMarkstein>, static_cast<int>(grid), st,
+                                    packed, sf, nblk, global_scale, out));
+    return launch_status(launch(nvfp4_dequantize_kernel<kDivIeee>, static_cast<int>(grid), st, packed, sf,
+                                nblk, global_scale, out));
+}
+
+int moe_nvfp4_traffic_floor(const uint16_t* in, int64_t rows, int64_t width, int32_t kind,
+                            uint8_t* packed, uint8_t* sf, moe_nvfp4_stream_t stream) {
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (kind < MOE_NVFP4_TRAFFIC_FUSED || kind > MOE_NVFP4_TRAFFIC_READ) return MOE_NVFP4_EMODE;
+    int rc;
+    DeviceInfo di;
+    if (kind == MOE_NVFP4_TRAFFIC_EMPTY) {
+        if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+        return launch_status(launch_shaped(empty_kernel, dim3(1), 32, st));
+    }
+    if (kind == MOE_NVFP4_TRAFFIC_READ) {
+        if (rows < 0) return MOE_NVFP4_ESIZE;
+        if (width <= 0 || width % 16 != 0) return MOE_NVFP4_EWIDTH;
+        if (rows > 0 && width > INT64_MAX / 2 / rows) return MOE_NVFP4_ESIZE;
+        if (rows == 0) return MOE_NVFP4_OK;
+        if (in == nullptr || packed == nullptr) return MOE_NVFP4_ENULL;
+        if (!aligned(in, 32) || !aligned(packed, 4)) return MOE_NVFP4_EALIGN;
+        if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+        return launch_status(launch(read_sweep_kernel, di.sms * 4, st, reinterpret_cast<const uint32_t*>(in),
+                                    rows * width / 16, reinterpret_cast<uint32_t*>(packed)));
+    }
+    const bool fused = kind == MOE_NVFP4_TRAFFIC_FUSED;
+    if ((rc = check_common(in, rows, width, fused ? 4 : 2, packed, sf)) != MOE_NVFP4_OK || rows == 0) return rc;
+    if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    const int64_t nblk = rows * (width / 16);
+    const uint32_t* in32 = reinterpret_cast<const uint32_t*>(in);
+    // the launch shape the step itself takes for this size
+    if (fused) {
+        if (small_problem(nblk, di.sms, di.occ[1][0]))
+            return launch_status(launch_shaped(traffic_small_kernel<16>, dim3(small_grid(nblk)), kSmallThreads,
+                                               st, in32, nblk, packed, sf));
+        return launch_status(launch(fused_traffic_kernel, grid_for(nblk, di.sms, di.occ_traffic[0]), st, in32,
+                                    nblk, packed, sf));
+    }
+    if (small_problem(nblk, di.sms, di.occ_quant[0]))
+        return launch_status(launch_shaped(traffic_small_kernel<8>, dim3(small_grid(nblk)), kSmallThreads, st,
+                                           in32, nblk, packed, sf));
+    return launch_status(launch(quantize_traffic_kernel, grid_for(nblk, di.sms, di.occ_traffic[1], kUnrollQuant),
+                                st, in32, nblk, packed, sf));
+}
+
+int moe_nvfp4_check_offsets(const int32_t* expert_offsets, int32_t num_experts, int64_t rows,
+                            const int32_t* out_offsets, int64_t out_rows, int32_t* status,
+                            moe_nvfp4_stream_t stream) {
+    if (num_experts < 0 || rows < 0 || out_rows < 0) return MOE_NVFP4_ESIZE;
+    if (expert_offsets == nullptr || status == nullptr) return MOE_NVFP4_ENULL;
+    if (!aligned(expert_offsets, 4) || !aligned(status, 4) || (out_offsets != nullptr && !aligned(out_offsets, 4)))
+        return MOE_NVFP4_EALIGN;
+    const int64_t tiles_x = (static_cast<int64_t>(num_experts) + 1 + kCheckTile - 1) / kCheckTile;
+    const int64_t tiles_y = out_offsets == nullptr ? 1 : (static_cast<int64_t>(num_experts) + kCheckTile - 1) / kCheckTile;
+    if (tiles_y > 65535) return MOE_NVFP4_ESIZE;
+    DeviceInfo di;
+    int rc;
+    if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
+    return launch_status(launch_shaped(check_offsets_kernel,
+                                       dim3(static_cast<unsigned>(tiles_x), static_cast<unsigned>(tiles_y < 1 ? 1 : tiles_y)),
+                                       kCheckTile, reinterpret_cast<cudaStream_t>(stream), expert_offsets,
+                                       static_cast<int>(num_experts), rows, out_offsets, out_rows, status));
 }
 
 double moe_swiglu_nvfp4_window(float clamp_L) { return window_for(clamp_L); }
@@ -1412,6 +1850,6 @@ const char* moe_nvfp4_strerror(int code) {
     }
 }
 
-int moe_nvfp4_abi_version(void) { return 5; }
+int moe_nvfp4_abi_version(void) { return 6; }
 
 }  // extern "C"

@@ -44,7 +44,7 @@ def exe(tmp_path_factory):
 def test_c_program_gets_the_documented_error_codes(exe):
     out = subprocess.run([exe], capture_output=True, text=True, check=True, timeout=60).stdout.splitlines()
     # width not a multiple of 16, negative rows, null input, bad clamp, rows == 0, ABI version
-    assert [int(v) for v in out[0].split()] == [-2, -4, -1, -5, 0, 5]
+    assert [int(v) for v in out[0].split()] == [-2, -4, -1, -5, 0, 6]
     assert "16" in out[1]                                 # the message names the width rule
 
 

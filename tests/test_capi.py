@@ -45,7 +45,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert lib.moe_nvfp4_abi_version() == 5
+    assert lib.moe_nvfp4_abi_version() == 6
     for code in range(0, -10, -1):
         assert lib.moe_nvfp4_strerror(code)
     assert b"unknown" in lib.moe_nvfp4_strerror(-99)
@@ -178,3 +178,27 @@ def test_gemm_argument_errors(lib):
     assert w4(A16, A16, A2, 4, 256, 128, 7.0, A16, 1, A16, A16, NULL, S) == -3
     assert w4(A16, A16, A16, 4, 256, 128, 0.0, A16, 1, A16, A16, NULL, S) == -5
     assert w4(NULL, NULL, NULL, 0, 256, 128, 7.0, A16, 1, NULL, NULL, NULL, S) == 0
+
+
+def test_diagnostic_argument_errors(lib):
+    tf = lib.moe_nvfp4_traffic_floor
+    # (in, rows, width, kind, packed, sf, stream)
+    assert tf(A32, 4, 32, 9, A16, A16, S) == -9                 # unknown kind
+    assert tf(A32, 4, 32, -1, A16, A16, S) == -9
+    assert tf(A32, 4, 24, 0, A16, A16, S) == -2
+    assert tf(A16, 4, 32, 0, A16, A16, S) == -3                 # input 32-byte aligned
+    assert tf(A32, 4, 32, 1, NULL, A16, S) == -1
+    assert tf(A32, -1, 32, 3, A16, NULL, S) == -4
+    assert tf(NULL, 4, 32, 3, A16, NULL, S) == -1
+    assert tf(A32, 4, 32, 3, A2, NULL, S) == -3                 # sink 4-byte aligned
+    assert tf(NULL, 0, 32, 0, NULL, NULL, S) == 0
+    co = lib.moe_nvfp4_check_offsets
+    # (offsets, E, rows, out_offsets, out_rows, status, stream)
+    assert co(A16, -1, 4, NULL, 0, A16, S) == -4
+    assert co(A16, 2, -4, NULL, 0, A16, S) == -4
+    assert co(NULL, 2, 4, NULL, 0, A16, S) == -1
+    assert co(A16, 2, 4, NULL, 0, NULL, S) == -1
+    assert co(A2, 2, 4, NULL, 0, A16, S) == -3
+    assert co(A16, 2, 4, A2, 8, A16, S) == -3
+    assert co(A16, 2, 4, NULL, 0, A2, S) == -3
+    assert co(A16, 2 ** 31 - 1, 4, A16, 8, A16, S) == -4       # too many segments for the overlap test
