@@ -14,9 +14,17 @@ Workloads (rows x width, distribution, clamp L):
   prefill    gu [65536, 2*3072] ~ 0.5 * Student-t(3), 0.1% of values x100,
              5% of output 16-blocks zeroed (all 32 inputs), L = 10
   edge       gu [16384, 2*4096], 90% of output blocks ~ N(0, 1), 10% of
-             blocks structured (signed zeros, saturated gates with tiny ups
+             blocks adversarial (signed zeros, saturated gates with tiny ups
              reaching subnormal scales, clamp-boundary values, huge
-             magnitudes), L = 7
+             magnitudes, and blocks whose SwiGLU values sit on, or within a
+             few ulps of, FP8 scale ties and E2M1 half-step ties), L = 7
+  edge_quantize
+             x [16384, 4096] ~ N(0, 1) with 10% of the 16-blocks adversarial
+             (ties, subnormal scales, saturation at amax = 448 * 6, zeros):
+             the edge cases the clamp keeps out of the fused path
+The tie blocks come from a table (tests/golden/edge_adversarial_blocks.npz)
+written by a committed script with the oracle; this module only places its
+rows at seeded positions.
 Every generator takes a row count (and width) so tests can draw the same
 distributions at sizes the oracle finishes in seconds.
 """
@@ -171,15 +179,34 @@ def prefill_heavy_tail_quantize(rows=65536, K=3072, seed=3) -> Workload:
 
 
 EDGE_KINDS = ("signed_zero", "saturated_gate_tiny_up", "clamp_boundary", "huge", "structured")
+EDGE_TABLE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "tests", "golden",
+                          "edge_adversarial_blocks.npz")
+_edge_table = None
+
+
+def edge_table() -> dict:
+    """The adversarial blocks: "fused" [n, 32] interleaved BF16 bits (for
+    L = 7) and "quantize" [m, 16] BF16 bits. Raises if the table is missing:
+    the edge workloads are not built without it."""
+    global _edge_table
+    if _edge_table is None:
+        if not os.path.exists(EDGE_TABLE):
+            raise FileNotFoundError(f"{EDGE_TABLE} is missing (tests/golden/make_edge_adversarial_blocks.py)")
+        with np.load(EDGE_TABLE) as z:
+            _edge_table = {"fused": z["fused"].astype(np.uint16), "quantize": z["quantize"].astype(np.uint16),
+                           "fused_clamp_L": float(z["fused_clamp_L"])}
+    return _edge_table
 
 
 def edge_structured(rows=16384, I=4096, seed=4, L=7.0, adversarial_frac=0.10) -> Workload:
     """90% N(0,1) blocks; the rest one of EDGE_KINDS per output block. The
-    "structured" blocks are plain N(0,1) here; tests overwrite them with
-    near-tie values found by searching the oracle. meta["kinds"][r, b] is
-    the kind index + 1 (0 = plain)."""
+    "structured" blocks are rows of the adversarial table (for L = 7; at
+    another L they stay N(0,1)): SwiGLU values on or next to scale ties and
+    half-step ties. meta["kinds"][r, b] is the kind index + 1 (0 = plain)."""
     Lf = np.float32(L)
     nb = I // 16
+    tab = edge_table()
+    tie_blocks = bf16_to_f32(tab["fused"]) if L == tab["fused_clamp_L"] else None
 
     def fill(rng, n, r0):
         v = rng.standard_normal((n, 2 * I), dtype=np.float32)
@@ -209,12 +236,33 @@ def edge_structured(rows=16384, I=4096, seed=4, L=7.0, adversarial_frac=0.10) ->
         tmp[...] = (rng.choice(np.array([-1, 1], np.float32), tmp.shape)
                     * np.exp(rng.uniform(np.log(30.0), np.log(3e38), tmp.shape))).astype(np.float32)
         blocks[sel] = tmp
+        sel = kind == 5                          # table rows: ties and near-ties
+        if tie_blocks is not None and np.any(sel):
+            v.reshape(n, nb, 32)[sel] = tie_blocks[rng.integers(0, tie_blocks.shape[0], int(np.count_nonzero(sel)))]
         kinds_out[r0:r0 + n] = kind
         return bf16_bits(v)
 
     kinds_out = np.zeros((rows, nb), np.uint8)
     gu = _chunked(rows, 2 * I, seed, 6, fill)
     return Workload("edge", "fused", rows, I, gu, clamp_L=L, meta={"kinds": kinds_out})
+
+
+def edge_quantize(rows=16384, K=4096, seed=4, adversarial_frac=0.10) -> Workload:
+    """x ~ N(0, 1) with a fraction of the 16-blocks replaced by rows of
+    the adversarial quantize table. meta["adversarial"][r, b] marks them."""
+    tab = edge_table()["quantize"]
+    nb = K // 16
+
+    def fill(rng, n, r0):
+        v = bf16_bits(rng.standard_normal((n, K), dtype=np.float32)).reshape(n, nb, 16)
+        sel = rng.random((n, nb)) < adversarial_frac
+        v[sel] = tab[rng.integers(0, tab.shape[0], int(np.count_nonzero(sel)))]
+        marks[r0:r0 + n] = sel
+        return v.reshape(n, K)
+
+    marks = np.zeros((rows, nb), bool)
+    x = _chunked(rows, K, seed, 9, fill)
+    return Workload("edge_quantize", "quantize", rows, K, x, meta={"adversarial": marks})
 
 
 @dataclass
@@ -286,5 +334,6 @@ def make(name: str, **kw) -> Workload:
         "prefill": prefill_heavy_tail,
         "prefill_quantize": prefill_heavy_tail_quantize,
         "edge": edge_structured,
+        "edge_quantize": edge_quantize,
     }
     return table[name](**kw)

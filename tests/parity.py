@@ -132,38 +132,28 @@ def quantize_edge_blocks(rng, n_blocks: int) -> np.ndarray:
     return np.stack(blocks)
 
 
-def fused_near_tie_blocks(rng, n_blocks: int, L: float, gate_lo: float = -6.0):
-    """Interleaved BF16 blocks [n, 32] whose oracle SwiGLU values land as
-    close as BF16 (gate, up) pairs allow to rounding boundaries: the block
-    amax on 6 x an E4M3 value, or on 6 x the midpoint between two (a scale
-    tie, subnormal scales included), the other 15 outputs on half-step ties
-    (2k+1)/4 * d. For every target, every BF16 gate in [gate_lo, L + 1] is
-    paired with the two BF16 ups around target / silu(gate), and the pair
-    whose oracle value is nearest wins. Exact hits are rare (a BF16 up has
-    8 bits, so a gate lands within half an fp32 ulp of a target with
-    probability ~2^-16); most values end a few ulps from their boundary.
-    Returns (blocks, {"exact_hits", "median_rel_distance", "targets"})."""
+def _gate_table(L: float, gate_lo: float):
+    """Every BF16 gate in [gate_lo, L + 1] whose oracle silu is >= 2^-6 in
+    magnitude, with that silu value (float64)."""
     allg = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
     gf = W.bf16_to_f32(allg)
     sel = np.isfinite(gf) & (gf >= gate_lo) & (gf <= L + 1.0)
     gf = gf[sel]
     sig = oracle.swiglu_clamped_array(gf, np.ones_like(gf), L).astype(np.float64)
     keep = np.abs(sig) >= 2.0 ** -6
-    gf, sig = gf[keep], sig[keep]
+    return gf[keep], sig[keep]
 
-    targets = np.zeros((n_blocks, 16))
-    for n in range(n_blocks):
-        code = int(rng.integers(1, 0x48))         # scales up to 3.75: |y| <= L silu(L)
-        d = e4m3_value(code)
-        amax = 3 * (d + e4m3_value(code + 1)) if n % 3 == 0 else 6 * d
-        targets[n, 0] = amax
-        targets[n, 1:] = (2 * rng.integers(0, 12, 15) + 1) / 4 * d
-    targets *= np.where(rng.integers(0, 2, targets.shape) == 1, -1.0, 1.0)
-    flat = targets.ravel()
+
+def nearest_pairs(targets, L: float, gate_lo: float = -6.0):
+    """For every target value, the BF16 (gate, up) pair whose oracle SwiGLU
+    lies nearest to it: every BF16 gate in [gate_lo, L + 1] is paired with
+    the two BF16 ups around target / silu(gate). Returns (gates, ups,
+    distances), float32 / float32 / float64 arrays shaped like targets."""
+    gf, sig = _gate_table(L, gate_lo)
+    flat = np.asarray(targets, np.float64).ravel()
     best_g = np.zeros(flat.size, np.float32)
     best_u = np.zeros(flat.size, np.float32)
-    hits = 0
-    rel_dist = np.zeros(flat.size)
+    best_all = np.full(flat.size, np.inf)
     for c0 in range(0, flat.size, 256):
         t = flat[c0:c0 + 256]
         ustar = t[:, None] / sig[None, :]
@@ -182,16 +172,89 @@ def fused_near_tie_blocks(rng, n_blocks: int, L: float, gate_lo: float = -6.0):
             rows = np.nonzero(better)[0]
             best_g[c0 + rows] = gf[j[rows]]
             best_u[c0 + rows] = U[rows, j[rows]]
-        hits += int(np.count_nonzero(best_d == 0))
-        rel_dist[c0:c0 + t.size] = best_d / np.abs(t)
-    out = np.zeros((n_blocks, 32), np.uint16)
-    for n in range(n_blocks):
+        best_all[c0:c0 + t.size] = best_d
+    shape = np.shape(targets)
+    return best_g.reshape(shape), best_u.reshape(shape), best_all.reshape(shape)
+
+
+def _blocks_from_pairs(rng, g, u):
+    """[n, 16] gate / up values -> interleaved BF16 blocks [n, 32], the 16
+    outputs of each block in a random order."""
+    n = g.shape[0]
+    out = np.zeros((n, 32), np.uint16)
+    for k in range(n):
         perm = rng.permutation(16)
-        gate = W.bf16_bits(best_g[16 * n:16 * n + 16][perm])
-        up = W.bf16_bits(best_u[16 * n:16 * n + 16][perm])
-        out[n] = W.interleave_gate_up(gate[None, :], up[None, :])[0]
-    return out, {"exact_hits": hits, "median_rel_distance": float(np.median(rel_dist)),
-                 "targets": int(flat.size)}
+        out[k] = W.interleave_gate_up(W.bf16_bits(g[k][perm])[None, :], W.bf16_bits(u[k][perm])[None, :])[0]
+    return out
+
+
+def fused_near_tie_blocks(rng, n_blocks: int, L: float, gate_lo: float = -6.0):
+    """Interleaved BF16 blocks [n, 32] whose oracle SwiGLU values land as
+    close as BF16 (gate, up) pairs allow to rounding boundaries: the block
+    amax on 6 x an E4M3 value, or on 6 x the midpoint between two (a scale
+    tie, subnormal scales included), the other 15 outputs on half-step ties
+    (2k+1)/4 * d. Exact hits are rare (exact_tie_pairs: an exhaustive count);
+    most values end a few ulps from their boundary, inside the fused
+    kernel's decision window.
+    Returns (blocks, {"exact_hits", "median_rel_distance", "targets"})."""
+    targets = np.zeros((n_blocks, 16))
+    for n in range(n_blocks):
+        code = int(rng.integers(1, 0x48))         # scales up to 3.75: |y| <= L silu(L)
+        d = e4m3_value(code)
+        amax = 3 * (d + e4m3_value(code + 1)) if n % 3 == 0 else 6 * d
+        targets[n, 0] = amax
+        targets[n, 1:] = (2 * rng.integers(0, 12, 15) + 1) / 4 * d
+    targets *= np.where(rng.integers(0, 2, targets.shape) == 1, -1.0, 1.0)
+    g, u, dist = nearest_pairs(targets, L, gate_lo)
+    out = _blocks_from_pairs(rng, g, u)
+    return out, {"exact_hits": int(np.count_nonzero(dist == 0)),
+                 "median_rel_distance": float(np.median(dist / np.abs(targets))),
+                 "targets": int(targets.size)}
+
+
+def exact_tie_pairs(L: float, min_abs: float = 2.0 ** -12):
+    """Every BF16 pair (gate in [-16, L + 1] with |gate| >= 2^-14, up in
+    [2^-16, L]) whose oracle SwiGLU y (|y| >= min_abs) sits exactly on a
+    half-step tie (2k+1)/4 * d of an E4M3 scale d (k = 0..11), found by
+    evaluating all of them. Returns a list of (gate, up, y, code, k); ups of
+    the other sign give -y (the clamp is symmetric)."""
+    allb = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    f = W.bf16_to_f32(allb)
+    g = f[np.isfinite(f) & (f >= -16) & (f <= L + 1) & (np.abs(f) >= 2.0 ** -14)]
+    u = f[np.isfinite(f) & (f > 0) & (f <= L) & (f >= 2.0 ** -16)]
+    G = np.repeat(g, u.size)
+    U = np.tile(u, g.size)
+    y = oracle.swiglu_clamped_array(G, U, L)
+    # a tie value has at most 9 significant bits: (2k+1) <= 23 times a 4-bit d
+    short = ((y.view(np.uint32) & 0x7FFF) == 0) & (np.abs(y) >= min_abs)
+    d = {c: e4m3_value(c) for c in range(1, 0x7f)}
+    found = []
+    for gi, ui, yi in zip(G[short], U[short], y[short]):
+        for k in range(12):
+            want = abs(float(yi)) * 4 / (2 * k + 1)
+            for c, dc in d.items():
+                if dc == want:
+                    found.append((float(gi), float(ui), float(yi), c, k))
+    return found
+
+
+def fused_exact_tie_blocks(rng, n_blocks: int, L: float, pairs, gate_lo: float = -6.0):
+    """Blocks around the exact tie pairs (exact_tie_pairs): the amax on
+    6 x the pair's scale d (nearest pair), and the other 15 outputs the pair
+    itself with random signs, each exactly on its half-step tie under d."""
+    if not pairs:
+        return np.zeros((0, 32), np.uint16)
+    g = np.zeros((n_blocks, 16), np.float32)
+    u = np.zeros((n_blocks, 16), np.float32)
+    amax_t = np.zeros(n_blocks)
+    for n in range(n_blocks):
+        pg, pu, _, code, _ = pairs[n % len(pairs)]
+        amax_t[n] = 6 * e4m3_value(code)
+        g[n, 1:] = pg
+        u[n, 1:] = np.where(rng.integers(0, 2, 15) == 1, -pu, pu)
+    ag, au, _ = nearest_pairs(amax_t, L, gate_lo)
+    g[:, 0], u[:, 0] = ag, au
+    return _blocks_from_pairs(rng, g, u)
 
 
 def near_bf16_midpoint_blocks(rng, n_blocks: int, L: float, max_ulps: int = 8,

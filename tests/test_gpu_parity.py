@@ -389,7 +389,22 @@ def test_repeat_runs_are_identical():
 # full-size workloads, as the benchmark launches them: sampled blocks
 # ---------------------------------------------------------------------------
 
+def adversarial_positions(w):
+    """(rows, blocks) of every adversarial table block the edge workloads
+    place (ties and near-ties of the fused path; ties, saturation and zeros
+    of quantize-only), or empty arrays."""
+    if w.name == "edge":
+        pos = np.argwhere(w.meta["kinds"] == W.EDGE_KINDS.index("structured") + 1)
+    elif w.name == "edge_quantize":
+        pos = np.argwhere(w.meta["adversarial"])
+    else:
+        pos = np.zeros((0, 2), np.int64)
+    return pos[:, 0], pos[:, 1]
+
+
 def _sampled_check(w, gp, gs, n_sample=60000, seed=0):
+    """Sampled blocks, every block of the first and last active rows, and
+    every adversarial table block of the edge workloads."""
     rng = np.random.default_rng(seed)
     nb = w.width // 16
     r0 = 0 if w.offsets is None else int(w.offsets[0])
@@ -397,8 +412,9 @@ def _sampled_check(w, gp, gs, n_sample=60000, seed=0):
     rows = rng.integers(r0, r1, n_sample)
     blks = rng.integers(0, nb, n_sample)
     edge_rows = np.repeat([r0, r1 - 1], nb)
-    rows = np.concatenate([rows, edge_rows])
-    blks = np.concatenate([blks, np.tile(np.arange(nb), 2)])
+    adv_r, adv_b = adversarial_positions(w)
+    rows = np.concatenate([rows, edge_rows, adv_r])
+    blks = np.concatenate([blks, np.tile(np.arange(nb), 2), adv_b])
     if w.kind == "quantize":
         rp, rs = oracle.quantize_nvfp4_blocks(w.data, rows, blks)
         gpb = gp.reshape(w.rows, nb, 8)[rows, blks]
@@ -476,9 +492,11 @@ def test_inputs_beyond_2_31_elements_sampled(kind):
             assert np.array_equal(gd[k], oracle.dequantize_nvfp4(gp[k:k + 1], gs[k:k + 1], 1.0)[0]), check[k]
 
 
-@pytest.mark.parametrize("name", ["ragged", "prefill", "edge", "prefill_quantize"])
+@pytest.mark.parametrize("name", ["ragged", "prefill", "edge", "prefill_quantize", "edge_quantize"])
 def test_full_size_workloads_sampled(name):
     w = W.make(name)
+    if name == "edge":                                    # the tie blocks are in it
+        assert len(adversarial_positions(w)[0]) > 80000
     if w.kind == "quantize":
         gp, gs = run_quantize(w.data)
     else:

@@ -88,3 +88,39 @@ def test_algorithmic_bytes():
     assert w.algorithmic_bytes() == 4 * 9344
     q = W.quantize_normal(rows=4, K=2048)
     assert q.algorithmic_bytes() == 4 * 5248
+
+
+def test_edge_table_is_what_its_script_writes():
+    """The committed adversarial table is exactly the output of its script
+    (seeded, oracle only), so no stored input came from anywhere else."""
+    import importlib.util
+    import os
+    here = os.path.dirname(os.path.abspath(__file__))
+    spec = importlib.util.spec_from_file_location(
+        "make_edge", os.path.join(here, "golden", "make_edge_adversarial_blocks.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    fused, quant, _, pairs, exact = mod.build_table()
+    tab = W.edge_table()
+    assert np.array_equal(tab["fused"], fused) and np.array_equal(tab["quantize"], quant)
+    assert exact.shape[0] == (mod.N_EXACT if pairs else 0)
+
+
+def test_edge_workloads_place_table_rows():
+    tab = W.edge_table()
+    w = W.edge_structured(rows=256, I=1024)
+    nb = w.width // 16
+    blocks = w.data.reshape(w.rows, nb, 32)
+    pos = np.argwhere(w.meta["kinds"] == W.EDGE_KINDS.index("structured") + 1)
+    assert len(pos) > 50
+    rows_of_table = {bytes(r) for r in tab["fused"]}
+    assert all(bytes(blocks[r, b]) in rows_of_table for r, b in pos)
+    q = W.edge_quantize(rows=256, K=1024)
+    qb = q.data.reshape(q.rows, -1, 16)
+    qrows = {bytes(r) for r in tab["quantize"]}
+    marks = np.argwhere(q.meta["adversarial"])
+    assert 0.05 < len(marks) / q.meta["adversarial"].size < 0.15
+    assert all(bytes(qb[r, b]) in qrows for r, b in marks)
+    # amax = 448 * 6 and beyond (saturating scales) occur in the quantize table
+    amax = np.abs(W.bf16_to_f32(tab["quantize"])).max(axis=1)
+    assert np.any(amax >= 6 * 448)
