@@ -317,14 +317,37 @@ def launch_percentiles(torch, calls, n: int, stream):
     return [round(float(v), 2) for v in np.percentile(us, [10, 50, 90])]
 
 
+def e2e_chunks(w, chunks: int):
+    """Row ranges of the e2e pipeline. With expert offsets the chunks are
+    groups of whole expert segments (each call gets its group's slice of
+    the device offsets, so the ragged path runs end to end); otherwise
+    equal row ranges. Returns [(row0, row1, expert0, expert1)]."""
+    if w.offsets is None:
+        b = np.linspace(0, w.rows, chunks + 1).astype(np.int64)
+        return [(int(a), int(c), 0, 0) for a, c in zip(b[:-1], b[1:])]
+    off = w.offsets.astype(np.int64)
+    E = off.shape[0] - 1
+    out, e0 = [], 0
+    for k in range(1, chunks + 1):
+        target = off[0] + (off[-1] - off[0]) * k // chunks
+        e1 = E if k == chunks else int(np.searchsorted(off, target, side="left"))
+        e1 = max(e1, e0)
+        if e1 > e0:
+            out.append((int(off[e0]), int(off[e1]), e0, e1))
+        e0 = e1
+    return out
+
+
 def e2e_measure(torch, lib, w, stream, steps: int, chunks: int = 8):
     """Through the public C-ABI call with HOST buffers, pipelined the way a
-    streaming caller would: the rows are split into `chunks` ranges; each is
-    copied from pinned host memory on an upload stream, processed by one
-    C-ABI call on the compute stream, and its outputs are read back on a
-    download stream, so transfers in both directions overlap the kernels.
-    Every step moves the whole input and the whole output; the timed region
-    spans the first upload to the last download."""
+    streaming caller would: the active rows are split into `chunks` ranges
+    (whole expert segments when the workload has offsets); each is copied
+    from pinned host memory on an upload stream, processed by one C-ABI call
+    (with its slice of the device expert offsets) on the compute stream, and
+    its outputs are read back on a download stream, so transfers in both
+    directions overlap the kernels. Every step moves every active row's input
+    and output; the timed region spans the first upload to the last
+    download."""
     P = ctypes.c_void_p
     h_in = torch.from_numpy(w.data.view(np.int16)).pin_memory()
     h_packed = torch.empty((w.rows, w.width // 2), dtype=torch.uint8).pin_memory()
@@ -332,31 +355,33 @@ def e2e_measure(torch, lib, w, stream, steps: int, chunks: int = 8):
     d_in = torch.empty_like(h_in, device="cuda")
     d_packed = torch.empty_like(h_packed, device="cuda")
     d_sf = torch.empty_like(h_sf, device="cuda")
-    r0 = 0 if w.offsets is None else int(w.offsets[0])
-    r1 = w.rows if w.offsets is None else int(w.offsets[-1])
-    bounds = np.linspace(r0, r1, chunks + 1).astype(np.int64)
+    d_off = None if w.offsets is None else torch.from_numpy(w.offsets).cuda()
+    parts = e2e_chunks(w, chunks)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     in_w = 2 * w.width if w.kind == "fused" else w.width          # BF16 values per input row
     calls = []
-    for a, b in zip(bounds[:-1], bounds[1:]):
-        a, b = int(a), int(b)
+    for a, b, e0, e1 in parts:
         if w.kind == "quantize":
             calls.append(DirectCall(lib.moe_nvfp4_quantize,
                                     (P(d_in.data_ptr() + a * in_w * 2), b - a, w.width,
                                      P(d_packed.data_ptr() + a * (w.width // 2)),
                                      P(d_sf.data_ptr() + a * (w.width // 16)), P(stream.cuda_stream))))
-        else:
+        elif d_off is None:
             calls.append(DirectCall(lib.moe_swiglu_nvfp4_quantize,
                                     (P(d_in.data_ptr() + a * in_w * 2), b - a, w.width, ctypes.c_float(w.clamp_L),
                                      P(0), ctypes.c_int32(0), P(d_packed.data_ptr() + a * (w.width // 2)),
                                      P(d_sf.data_ptr() + a * (w.width // 16)), P(stream.cuda_stream))))
+        else:                                     # whole buffers, this group's offsets
+            calls.append(DirectCall(lib.moe_swiglu_nvfp4_quantize,
+                                    (P(d_in.data_ptr()), w.rows, w.width, ctypes.c_float(w.clamp_L),
+                                     P(d_off.data_ptr() + 4 * e0), ctypes.c_int32(e1 - e0),
+                                     P(d_packed.data_ptr()), P(d_sf.data_ptr()), P(stream.cuda_stream))))
     ev_in = [torch.cuda.Event() for _ in calls]
     ev_k = [torch.cuda.Event() for _ in calls]
     ev_out = [torch.cuda.Event() for _ in calls]
 
     def step(first: bool):
-        for i, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
-            a, b = int(a), int(b)
+        for i, (a, b, _, _) in enumerate(parts):
             if not first:
                 s_in.wait_event(ev_k[i])               # the previous step's kernel read this range
             with torch.cuda.stream(s_in):
@@ -388,9 +413,10 @@ def e2e_measure(torch, lib, w, stream, steps: int, chunks: int = 8):
     ev1.record(s_in)
     torch.cuda.synchronize()
     secs = ev0.elapsed_time(ev1) / 1e3
-    h2d = (r1 - r0) * in_w * 2
-    d2h = (r1 - r0) * (w.width // 2 + w.width // 16)
-    return secs, h2d, d2h
+    rows = sum(b - a for a, b, _, _ in parts)
+    h2d = rows * in_w * 2
+    d2h = rows * (w.width // 2 + w.width // 16)
+    return secs, h2d, d2h, len(parts)
 
 
 def describe(w) -> str:
@@ -492,18 +518,65 @@ def cpu_baseline_all_cores(w):
             "rows_per_s": (r1 - r0) / secs}
 
 
-def small_config_extras(torch, lib, W, name: str, stream, per_cold):
-    """The small configs fit in L2 and a single cold launch is latency-bound;
-    beside its cold per-launch percentiles, the hot-L2 back-to-back mean and
-    a CUDA graph of 100 launches, each labelled."""
+class L2Flush:
+    """Evicts the L2 before a cold launch. "read" sweeps a buffer of twice
+    the L2 with the library's read-only kernel, leaving clean lines (nothing
+    to write back when the next kernel misses); "fill" writes the buffer
+    with torch's fill_, leaving the L2 full of dirty lines that the next
+    kernel's misses must write back first (what an application that just
+    wrote other data would see)."""
+
+    def __init__(self, torch, lib, stream):
+        P = ctypes.c_void_p
+        self.buf = torch.ones(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+        self.sink = torch.zeros(4, dtype=torch.uint8, device="cuda")
+        self.read = DirectCall(lib.moe_nvfp4_traffic_floor,
+                               (P(self.buf.data_ptr()), 2 * L2_BYTES // 32, 16, 3, P(self.sink.data_ptr()),
+                                P(0), P(stream.cuda_stream)))
+        self.fill = lambda: self.buf.fill_(1)
+
+
+def cold_launches(torch, stream, calls: dict, flush, n: int) -> dict:
+    """Each call in `calls` launched n times, each launch after `flush` and
+    between its own event pair on the launching stream; the calls take turns
+    so that drift affects them alike. Returns seconds per launch by name."""
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)] for k in calls}
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            for k, c in calls.items():
+                flush()
+                ev[k][i][0].record(stream)
+                c()
+                ev[k][i][1].record(stream)
+    torch.cuda.synchronize()
+    return {k: [a.elapsed_time(b) / 1e3 for a, b in v] for k, v in ev.items()}
+
+
+def small_config(torch, lib, W, name: str, stream, flush: L2Flush, peak: float, n: int = 60) -> dict:
+    """A workload that fits in L2 (configs 1 and 2), as single cold launches:
+    the median launch after a read flush, beside the two floors measured the
+    same way in the same loop -- a launch that does nothing, and a kernel
+    with the step's loads and stores and none of its arithmetic in the
+    step's own launch shape -- and the median after a fill flush. Then the
+    hot-L2 graph of 100 launches (the input resident in L2; not HBM)."""
+    P = ctypes.c_void_p
     w = W.make(name)
     srcs, packed, sf, off = device_buffers(w, torch, 1)
+    s = P(stream.cuda_stream)
     call = make_call(lib, w, srcs[0], packed, sf, off, stream)
+    packed2, sf2 = torch.empty_like(packed), torch.empty_like(sf)
+    kind = 0 if w.kind == "fused" else 1
+    copy = DirectCall(lib.moe_nvfp4_traffic_floor, (P(srcs[0].data_ptr()), w.rows, w.width, kind,
+                                                    P(packed2.data_ptr()), P(sf2.data_ptr()), s))
+    empty = DirectCall(lib.moe_nvfp4_traffic_floor, (P(0), 0, 0, 2, P(0), P(0), s))
     with torch.cuda.stream(stream):
-        _, per_hot, _, _ = time_steps(torch, [call], 200, 20, stream)
-        for _ in range(3):
-            call()
+        for _ in range(5):
+            call(), copy(), empty(), flush.read()
     torch.cuda.synchronize()
+    t = cold_launches(torch, stream, {"step": call, "copy": copy, "empty": empty}, flush.read, n)
+    t_fill = cold_launches(torch, stream, {"step": call}, flush.fill, n)["step"]
+    med = {k: statistics.median(v) for k, v in t.items()}
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for _ in range(100):
@@ -512,22 +585,82 @@ def small_config_extras(torch, lib, W, name: str, stream, per_cold):
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(10):
             g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-    graph_us = e0.elapsed_time(e1) * 1e3 / 1000
-    q = np.percentile(np.asarray(per_cold) * 1e6, [10, 50, 90])
     nbytes = w.algorithmic_bytes()
-    return {"cold_launch_us_p10_p50_p90": [round(float(v), 2) for v in q],
-            "hot_l2_back_to_back_us": round(statistics.fmean(per_hot) * 1e6, 2),
-            "hot_l2_gbs": round(nbytes / statistics.fmean(per_hot) / 1e9, 1),
-            "cuda_graph_100_launches_us_per_launch": round(graph_us, 2),
-            "cuda_graph_gbs": round(nbytes / (graph_us * 1e-6) / 1e9, 1),
-            "note": "hot-L2 and graph numbers reuse one input resident in L2 (not an HBM measurement)"}
+    return {"cold_us": round(med["step"] * 1e6, 2), "floor_copy_us": round(med["copy"] * 1e6, 2),
+            "floor_empty_us": round(med["empty"] * 1e6, 2),
+            "vs_copy_floor": round(med["step"] / med["copy"], 3),
+            "gbs": round(nbytes / med["step"] / 1e9, 1), "frac": round(nbytes / med["step"] / 1e9 / peak, 4),
+            "cold_us_fill_flush": round(statistics.median(t_fill) * 1e6, 2),
+            "hot_graph_us": round(e0.elapsed_time(e1) * 1e3 / 1000, 2)}
+
+
+def traffic_floor_us(torch, lib, w, srcs, stream, steps: int) -> float:
+    """Back-to-back mean launch time of the step's loads and stores without
+    its arithmetic, in its launch shape, over the same alternating inputs
+    (rows of the workload's active range; the offsets only bound it)."""
+    P = ctypes.c_void_p
+    r0 = 0 if w.offsets is None else int(w.offsets[0])
+    rows = w.active_rows
+    in_w = 2 * w.width if w.kind == "fused" else w.width
+    kind = 0 if w.kind == "fused" else 1
+    packed = torch.empty((rows, w.width // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((rows, w.width // 16), dtype=torch.uint8, device="cuda")
+    calls = [DirectCall(lib.moe_nvfp4_traffic_floor,
+                        (P(x.data_ptr() + r0 * in_w * 2), rows, w.width, kind, P(packed.data_ptr()),
+                         P(sf.data_ptr()), P(stream.cuda_stream))) for x in srcs]
+    with torch.cuda.stream(stream):
+        _, per, _, _ = time_steps(torch, calls, steps, 5, stream)
+    return statistics.fmean(per)
+
+
+def large_config(torch, lib, M, W, name: str, steps: int, warmup: int, stream, peak: float,
+                 timed=None) -> dict:
+    """A workload larger than L2, back to back (two input copies
+    alternating): mean launch, the isolated per-launch median, and the
+    traffic floor. `timed` reuses the headline's timed region."""
+    if timed is None:
+        timed = run_workload(torch, lib, M, W, name, steps, warmup, stream)
+    w, total_s, per, _, _, keep = timed
+    srcs, calls = keep[0], keep[4]
+    p50 = launch_percentiles(torch, calls, 50, stream)[1] * 1e-6
+    floor = traffic_floor_us(torch, lib, w, srcs, stream, min(steps, 200))
+    mean_s = statistics.fmean(per)
+    nbytes = w.algorithmic_bytes()
+    return {"us": round(mean_s * 1e6, 2), "gbs": round(nbytes / mean_s / 1e9, 1),
+            "frac": round(nbytes / mean_s / 1e9 / peak, 4), "p50_us": round(p50 * 1e6, 2),
+            "p50_frac": round(nbytes / p50 / 1e9 / peak, 4), "floor_us": round(floor * 1e6, 2)}
+
+
+def reevaluation_rates(torch, lib, W, name: str) -> dict:
+    """How often the fused kernel's exact path ran on a workload (the counted
+    variant, one launch): scale decisions per block, nibble decisions per
+    element."""
+    P = ctypes.c_void_p
+    w = W.make(name)
+    x = torch.from_numpy(w.data.view(np.int16)).cuda()
+    packed = torch.empty((w.rows, w.width // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((w.rows, w.width // 16), dtype=torch.uint8, device="cuda")
+    cnt = torch.zeros(3, dtype=torch.int64, device="cuda")
+    off = None if w.offsets is None else torch.from_numpy(w.offsets).cuda()
+    rc = lib.moe_swiglu_nvfp4_quantize_counted(P(x.data_ptr()), w.rows, w.width, ctypes.c_float(w.clamp_L),
+                                               P(0 if off is None else off.data_ptr()),
+                                               0 if off is None else off.shape[0] - 1, P(packed.data_ptr()),
+                                               P(sf.data_ptr()), P(cnt.data_ptr()),
+                                               P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    blocks, scales, nibbles = (int(v) for v in cnt.cpu())
+    return {"scale_reeval_per_block": float(f"{scales / max(blocks, 1):.3g}"),
+            "nibble_reeval_per_elem": float(f"{nibbles / max(16 * blocks, 1):.3g}")}
+
+
+NOMINAL_HBM_GBS = 8000.0          # the "about 8 TB/s" GB300 HBM3e figure the target is stated against
 
 
 def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str, traffic):
@@ -535,9 +668,9 @@ def roofline(bytes_per_launch: int, per_launch_s, peak_gbs: float, peak_src: str
     achieved = bytes_per_launch / mean_s / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
             "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
-            "peak_source": f"{peak_src} (hbm_gbs, burst copy)",
-            "launch_us_mean": round(mean_s * 1e6, 2),
-            "timing": "mean launch = timed region / launches (back-to-back on one stream)"}
+            "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+            "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "launch_us_mean": round(mean_s * 1e6, 2)}
 
 
 EXTENSION_CASES = ("two_level_scale", "bf16_compat", "bf16_compat_scaled", "padded_segments", "compact_writer",
@@ -797,6 +930,42 @@ def gemm_measurements(torch, lib, M, W, stream, hbm_peak: float, cases=GEMM_CASE
     return res
 
 
+def config_of(w, world: int) -> dict:
+    """The `config` object of both arms' JSON lines: the same workload gives
+    the same dict."""
+    return {"workload": describe(w), "rows": w.rows, "width": w.width, "experts": w.meta.get("experts"),
+            "bytes_per_step": w.algorithmic_bytes(),
+            "l2": f"inputs ({w.data.nbytes / 1e6:.0f} MB) larger than L2 (129 MB); 2 input copies alternate",
+            "parallelism": f"{world} independent replica(s), no collective on the path"}
+
+
+def measure_configs(torch, lib, M, W, args, stream, peak: float) -> dict:
+    """Configurations 1, 2, 4 and 5 of the step, compact: 1 and 2 (they fit
+    in L2) as cold single launches beside their floors; 4 and 5 back to back
+    with the isolated per-launch median and the traffic floor, also as
+    quantize-only on the same shape (where the scale saturates), and 5 with
+    the rates at which the exact path ran on its tie blocks. Configuration 3
+    is the headline, timed after these (on a GPU that has left its idle
+    clocks) and added by the caller."""
+    steps, warm = min(args.steps, 200), min(args.warmup, 20)
+    keep = ("us", "gbs", "frac", "p50_frac", "floor_us")
+    out = {}
+    flush = L2Flush(torch, lib, stream)
+    out["1"] = {"w": "quantize-only 128x2048", **small_config(torch, lib, W, "quantize", stream, flush, peak)}
+    out["2"] = {"w": "fused 512x2048", **small_config(torch, lib, W, "fused", stream, flush, peak)}
+    del flush
+    torch.cuda.empty_cache()
+    for key, name, label in (("4", "prefill", "prefill 65536x3072"), ("5", "edge", "edge 16384x4096")):
+        out[key] = {"w": label, **large_config(torch, lib, M, W, name, steps, warm, stream, peak)}
+        torch.cuda.empty_cache()
+    for key, name in (("4", "prefill_quantize"), ("5", "edge_quantize")):
+        r = large_config(torch, lib, M, W, name, steps, warm, stream, peak)
+        out[key]["quantize_only"] = {k: r[k] for k in keep}
+        torch.cuda.empty_cache()
+    out["5"].update(reevaluation_rates(torch, lib, W, "edge"))
+    return out
+
+
 def main_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -817,96 +986,65 @@ def main_ours(args):
     visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     gpu_id = visible[local] if local < len(visible) else str(local)
 
+    # the other configurations run in single-GPU runs only, before the
+    # headline's timed region
+    configs = None
+    if not args.no_extra and world == 1:
+        configs = measure_configs(torch, lib, M, W, args, stream, peak)
+
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    w, total_s, per, w0, w1, _keep = run_workload(torch, lib, M, W, args.workload, args.steps,
-                                                  args.warmup, stream)
+    headline = run_workload(torch, lib, M, W, args.workload, args.steps, args.warmup, stream)
     sampler.stop()
+    w, total_s, per, w0, w1, keep = headline
     clocks = sampler.summary(w0, w1)
-    pcts = launch_percentiles(torch, _keep[4], 100, stream)
-    del _keep
+    pcts = launch_percentiles(torch, keep[4], 100, stream)
     max_s = max_over_ranks(total_s)
     agg = aggregate_throughput(w.algorithmic_bytes(), w.active_rows, args.steps, max_s, world)
+    if configs is not None and w.name == "ragged":
+        head = large_config(torch, lib, M, W, w.name, args.steps, args.warmup, stream, peak, timed=headline)
+        configs = {"1": configs["1"], "2": configs["2"], "3": {"w": "ragged 32768x2048", **head},
+                   "4": configs["4"], "5": configs["5"]}
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    e2e_s, h2d, d2h = e2e_measure(torch, lib, w, stream, e2e_steps)
+    e2e_s, h2d, d2h, n_chunks = e2e_measure(torch, lib, w, stream, e2e_steps)
     e2e_max = max_over_ranks(e2e_s)
     e2e = {"value": round(world * w.algorithmic_bytes() * e2e_steps / e2e_max / 1e9, 2),
-           "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": e2e_steps, "rows_per_s": round(world * w.active_rows * e2e_steps / e2e_max, 1),
-           "how": "C-ABI calls on 8 row chunks, uploads / kernels / downloads pipelined on three streams; "
-                  "pinned host buffers"}
+           "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "how": f"{n_chunks} C-ABI calls per step on expert groups (device offsets), pinned host "
+                  "buffers, uploads/kernels/downloads pipelined on 3 streams"}
 
     kernel = "nvfp4_quantize_kernel" if w.kind == "quantize" else "swiglu_nvfp4_kernel"
     roof = roofline(w.algorithmic_bytes(), per, peak, peak_src, recorded_traffic(kernel, w.name))
     roof["launch_us_p10_p50_p90"] = pcts
-    roof["percentiles"] = "100 launches after the timed region, each between its own event pair"
 
-    # the extra measurements (other workloads, extensions, the L1 GEMM with
-    # 15 GB of weights per process) run in single-GPU runs only
-    extras = not args.no_extra and world == 1
-    others = {}
-    if extras:
-        for name, cold in (("fused", True), ("prefill", False), ("edge", False), ("quantize", True),
-                           ("prefill_quantize", False)):
-            if name == args.workload:
-                continue
-            steps = min(args.steps, 200)
-            ww, tot, per_o, _, _, keep = run_workload(torch, lib, M, W, name, steps,
-                                                      min(args.warmup, 20), stream,
-                                                      copies=1 if cold else 2, cold_small=cold)
-            pcts_o = None if cold else launch_percentiles(torch, keep[4], 50, stream)
-            del keep
-            torch.cuda.empty_cache()
-            mean_s = statistics.fmean(per_o)
-            others[name] = {
-                "rows": ww.rows, "width": ww.width, "kind": ww.kind,
-                "gbs": round(ww.algorithmic_bytes() / mean_s / 1e9, 1),
-                "frac_of_peak": round(ww.algorithmic_bytes() / mean_s / 1e9 / peak, 4),
-                "launch_us_mean": round(mean_s * 1e6, 2),
-                "l2": "flushed before every launch" if cold else "inputs larger than L2",
-            }
-            if pcts_o is not None:
-                others[name]["launch_us_p10_p50_p90"] = pcts_o
-            if cold:
-                others[name].update(small_config_extras(torch, lib, W, name, stream, per_o))
+    del headline, keep
+    torch.cuda.empty_cache()
 
-    extensions = {}
-    if extras:
-        extensions = extension_measurements(torch, lib, M, W, stream, min(args.steps, 200),
-                                            min(args.warmup, 20), peak)
-        extensions.update(gemm_measurements(torch, lib, M, W, stream, peak))
-        if "compact_flow" in extensions:
-            extensions["compact_flow"]["vs_fused_time"] = round(
-                extensions["compact_flow"]["launch_us_mean"] / (agg["ms_per_step"] * 1e3), 3)
-
-    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
-    cpu_all = cpu_baseline_all_cores(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w)
+        allc = cpu_baseline_all_cores(w)
+        cpu["all_cores"] = {"value": round(allc["value"], 3), "cores": allc["cores"]}
+        cpu["value"] = round(cpu["value"], 4)
+        cpu.pop("rows_per_s", None)
     if rank != 0:
         return
     line = {
         "metric": METRIC, "value": round(agg["gbs"], 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "io": "BF16 gate/up in; E2M1 nibbles and E4M3 scales out",
         "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": describe(w),
-                   "rows": w.rows, "width": w.width, "experts": w.meta.get("experts"),
-                   "bytes_per_step": w.algorithmic_bytes(),
-                   "l2": f"inputs ({w.data.nbytes / 1e6:.0f} MB) larger than L2 (129 MB); "
-                         "2 input copies alternate",
-                   "parallelism": f"{world} independent replica(s), no collective on the path"},
+        "config": config_of(w, world),
         "rows_per_s": round(agg["rows_per_s"], 1),
         "roofline": roof,
         "cpu_baseline": cpu,
-        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "workloads": others,
-        "extensions": extensions,
+        "configs": configs,
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 def main_reference(args):
@@ -947,7 +1085,8 @@ def main_reference(args):
         "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (oracle)",
         "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": describe(w), "rows_per_step_sample": n},
+        "config": config_of(w, world),
+        "rows_per_step_sample": n,
         "rows_per_s": round(n * args.steps / secs, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{n} consecutive active rows per step"},
@@ -964,15 +1103,17 @@ def parse(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["ragged", "fused", "prefill", "edge", "quantize", "prefill_quantize"])
+                    choices=["ragged", "fused", "prefill", "edge", "quantize", "prefill_quantize",
+                             "edge_quantize"])
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--gemm-case", default=None, metavar="EXPERTS:TOKENS",
+    ap.add_argument("--no-extra", action="store_true", help="skip the other configurations")
+    ap.add_argument("--gemm-case", default=None, metavar="EXPERTS:TOKENS|all",
                     help="time only the L1 GEMM with the step in its epilogue (top-8 routing, "
-                         "H=7168, I=2048) at this size and print its JSON record")
-    ap.add_argument("--extension", default=None, choices=EXTENSION_CASES,
+                         "H=7168, I=2048) at this size, or 'all' for the decode and prefill cases "
+                         "beside the unfused flows, and print its JSON record")
+    ap.add_argument("--extension", default=None, choices=EXTENSION_CASES + ("all",),
                     help="time only this extension of the activation step on the ragged "
-                         "workload and print its JSON record")
+                         "workload ('all': every one, and the compact flow) and print its JSON record")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     return ap.parse_args(argv)
@@ -988,10 +1129,13 @@ def main_gemm_case(args):
     lib = M.load_library()
     stream = torch.cuda.Stream()
     peak, _ = measured_peaks()
-    E, tokens = (int(v) for v in args.gemm_case.split(":"))
-    res = gemm_measurements(torch, lib, M, W, stream, peak,
-                            cases=((f"l1_gemm_{E}x{tokens}", E, tokens, args.steps),),
-                            warmup=args.warmup, unfused=False)
+    if args.gemm_case == "all":
+        res = gemm_measurements(torch, lib, M, W, stream, peak)
+    else:
+        E, tokens = (int(v) for v in args.gemm_case.split(":"))
+        res = gemm_measurements(torch, lib, M, W, stream, peak,
+                                cases=((f"l1_gemm_{E}x{tokens}", E, tokens, args.steps),),
+                                warmup=args.warmup, unfused=False)
     print(json.dumps(res), flush=True)
 
 
@@ -1005,8 +1149,13 @@ def main_extension_case(args):
     lib = M.load_library()
     stream = torch.cuda.Stream()
     peak, _ = measured_peaks()
-    res = extension_measurements(torch, lib, M, W, stream, args.steps, args.warmup, peak,
-                                 only=(args.extension,))
+    only = None if args.extension == "all" else (args.extension,)
+    res = extension_measurements(torch, lib, M, W, stream, args.steps, args.warmup, peak, only=only)
+    if only is None:                  # the compact flow beside the fused step on the same box
+        w, tot, per, _, _, keep = run_workload(torch, lib, M, W, "ragged", args.steps, args.warmup, stream)
+        del keep
+        res["fused_step_us"] = round(statistics.fmean(per) * 1e6, 2)
+        res["compact_flow"]["vs_fused_time"] = round(res["compact_flow"]["launch_us_mean"] / res["fused_step_us"], 3)
     print(json.dumps(res), flush=True)
 
 
