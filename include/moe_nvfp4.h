@@ -246,6 +246,9 @@ MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_counted(const uint16_t *gu, int64_t 
  *   status   optional DEVICE int32: the kernel writes a nonzero code there
  *            if one of its internal waits expired (about a second; a fault
  *            elsewhere on the device); untouched otherwise. May be NULL.
+ *            After an expired wait the kernel still waits (bounded) for
+ *            the TMA loads and MMAs it issued before it releases its TMEM
+ *            and exits.
  * Uses every SM (one CTA each, ~206 KB of shared memory and all 512 TMEM
  * columns of the SM), tcgen05 tensor cores and TMA. Allocates nothing.
  * Returns the codes above; MOE_NVFP4_ELAUNCH also when the CUDA driver's
@@ -306,18 +309,31 @@ MOE_NVFP4_API int moe_l1_gemm_w4_accumulators(const uint16_t *x, const uint8_t *
                                               const int32_t *expert_offsets, int32_t num_experts,
                                               float *acc, int32_t *status, moe_nvfp4_stream_t stream);
 
-/* Diagnostic of the failure path: moe_l1_gemm_swiglu_nvfp4's kernel with
- * its loads withheld (nothing ever completes the first stage) and every
- * internal wait limited to wait_cycles SM clock cycles (1000 ..
- * 2e9). Each role stops when its wait expires or another role's did: the
- * DEVICE int32 status (required here) receives the code of an expired wait
- * (1 producer / free stage, 2 MMA issuer / free accumulator, 3 MMA issuer /
- * loaded stage, 4 epilogue / finished accumulator), the TMEM is released,
- * and packed / sf are not written. The kernels run normally afterwards. */
+/* Diagnostic of the failure path of moe_l1_gemm_swiglu_nvfp4's kernel,
+ * with every internal wait limited to wait_cycles SM clock cycles (1000 ..
+ * 2e9) and one of two faults made on purpose (no GPU fault: a wait that can
+ * never complete):
+ *   MOE_L1_GEMM_SELFTEST_NO_LOADS    the producer issues no loads, so the
+ *                                    first MMA wait never completes
+ *   MOE_L1_GEMM_SELFTEST_NO_RELEASE  the epilogue never releases an
+ *                                    accumulator; the grid is one CTA, which
+ *                                    runs every tile, so the MMA issuer
+ *                                    stops after two tiles with loads and
+ *                                    MMAs issued before it
+ * Each role stops when its wait expires or another role's did: the DEVICE
+ * int32 status (required here) receives the code of an expired wait (1
+ * producer / free stage, 2 MMA issuer / free accumulator, 3 MMA issuer /
+ * loaded stage, 4 epilogue / finished accumulator; 8 if a load or MMA
+ * issued before the stop did not complete within the limit). Before the
+ * TMEM is released the producer waits for its issued loads and the MMA
+ * issuer for its issued MMAs (the same drain every abort takes); packed / sf
+ * are not written. The kernels run normally afterwards. MOE_NVFP4_EMODE for
+ * another mode. */
+enum { MOE_L1_GEMM_SELFTEST_NO_LOADS = 1, MOE_L1_GEMM_SELFTEST_NO_RELEASE = 2 };
 MOE_NVFP4_API int moe_l1_gemm_wait_selftest(const uint16_t *x, const uint16_t *w1, int64_t rows,
                                             int64_t H, int64_t I, const int32_t *expert_offsets,
                                             int32_t num_experts, uint8_t *packed, uint8_t *sf,
-                                            int32_t *status, int64_t wait_cycles,
+                                            int32_t *status, int64_t wait_cycles, int32_t mode,
                                             moe_nvfp4_stream_t stream);
 
 /*

@@ -92,7 +92,7 @@ def load_library():
     lib.moe_l1_gemm_w4_swiglu_nvfp4.restype = ctypes.c_int
     lib.moe_l1_gemm_w4_accumulators.argtypes = [P, P, P, I64, I64, I64, P, I32, P, P, P]
     lib.moe_l1_gemm_w4_accumulators.restype = ctypes.c_int
-    lib.moe_l1_gemm_wait_selftest.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P, I64, P]
+    lib.moe_l1_gemm_wait_selftest.argtypes = [P, P, I64, I64, I64, P, I32, P, P, P, I64, I32, P]
     lib.moe_l1_gemm_wait_selftest.restype = ctypes.c_int
     lib.moe_l1_gemm_bf16.argtypes = [P, P, I64, I64, I64, F, P, I32, I32, P, P, P]
     lib.moe_l1_gemm_bf16.restype = ctypes.c_int
@@ -441,11 +441,16 @@ def moe_l1_gemm_bf16(x, w1, expert_offsets, output: str = "gu", clamp_L: float =
     return out
 
 
+SELFTEST_MODES = {"no_loads": 1, "no_release": 2}
+
+
 def moe_l1_gemm_wait_selftest(x, w1, expert_offsets, status, wait_cycles: int, packed=None, sf=None,
-                              stream=None):
-    """Diagnostic of the failure path: the fused GEMM with its loads
-    withheld and every wait limited to wait_cycles; `status` (int32 CUDA
-    tensor [1]) receives the code of the wait that expired."""
+                              stream=None, mode: str = "no_loads"):
+    """Diagnostic of the failure path: the fused GEMM with every wait limited
+    to wait_cycles and a wait that can never complete (mode "no_loads": the
+    producer issues nothing; "no_release": the epilogue never frees an
+    accumulator, one CTA runs every tile); `status` (int32 CUDA tensor [1])
+    receives the code of the wait that expired."""
     x, w1, E, I, H = _gemm_operands(x, w1, expert_offsets)
     rows = x.shape[0]
     packed = _out(packed, (rows, I // 2), x.device, "packed")
@@ -455,7 +460,7 @@ def moe_l1_gemm_wait_selftest(x, w1, expert_offsets, status, wait_cycles: int, p
             ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w1.data_ptr()), rows, H, I,
             ctypes.c_void_p(expert_offsets.data_ptr()), E, ctypes.c_void_p(packed.data_ptr()),
             ctypes.c_void_p(sf.data_ptr()), ctypes.c_void_p(status.data_ptr()), int(wait_cycles),
-            _stream_ptr(stream))
+            SELFTEST_MODES[mode], _stream_ptr(stream))
     _check(rc, "moe_l1_gemm_wait_selftest")
     return packed, sf
 

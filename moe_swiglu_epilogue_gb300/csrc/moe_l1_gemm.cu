@@ -33,8 +33,11 @@
 //     half steps, E2M1 cast). The 8 blocks of a tile row are stored as 64
 //     packed bytes and 8 scale bytes.
 //   * Every wait on an mbarrier is bounded (about a second); on expiry the
-//     kernel records a status code, every role stops at its next wait, and
-//     the TMEM is released before the CTA exits.
+//     kernel records a status code and every role stops at its next wait.
+//     Before the TMEM is released and the CTA exits, the producer waits for
+//     the TMA loads it issued to land and the MMA issuer for the MMAs it
+//     issued to complete (both bounded), so no asynchronous write into this
+//     CTA's shared memory or TMEM outlives it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -82,7 +85,8 @@ struct GemmArgs {
     uint16_t* out_bf16;        // BF16 gu [rows, 2I] or SwiGLU [rows, I] outputs
     int32_t* status;           // optional: nonzero after a wait expired
     long long wait_cycles;     // limit of every mbarrier wait
-    int withhold_loads;        // diagnostic: the producer issues nothing
+    int selftest;              // diagnostic: 1 the producer issues nothing; 2 the epilogue
+                               // never releases an accumulator (one CTA runs every tile)
 };
 
 // What the epilogue writes: the NVFP4 activations (the fused step), the
@@ -96,6 +100,7 @@ struct SharedState {
     uint64_t empty[kStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
+    uint64_t drain;
     uint32_t tmem_base;
     int abort;
     int tile_prefix[kMaxGemmExperts + 1];    // M-tiles before expert e
@@ -131,6 +136,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* ab
             }
         }
     }
+}
+
+// Waits, bounded, for the phase of the given parity whatever the abort flag
+// says: the drain after an abort. False if the limit passed first.
+__device__ __forceinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    for (uint32_t n = 0;; n++) {
+        if (mbar_try(bar, parity)) return true;
+        if ((n & 31) == 31 && clock64() - t0 > limit) return false;
+    }
+}
+
+// Status code of a drain wait that expired (recorded only if no other code
+// was): an issued TMA load or MMA did not complete.
+constexpr int kDrainExpired = 8;
+
+__device__ __forceinline__ void drain_failed(int32_t* status) {
+    if (status != nullptr) atomicCAS(status, 0, kDrainExpired);
+}
+
+// The producer's drain: the last `stages` of the `issued` stage loads (a
+// stage's previous load completed before its next was issued) have landed.
+// Only the producer arrives on a full barrier, so a completed phase stays
+// completed.
+__device__ __forceinline__ void drain_loads(const uint64_t* full, int stages, uint32_t issued, long long limit,
+                                            int32_t* status) {
+    for (uint32_t j = issued > static_cast<uint32_t>(stages) ? issued - stages : 0u; j < issued; j++)
+        if (!mbar_wait_quiet(smem_u32(&full[j % stages]), (j / stages) & 1u, limit)) drain_failed(status);
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -173,6 +206,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(smem_u32(bar)) : "memory");
+}
+
+// The MMA issuer's drain: every MMA it issued has completed (one commit to
+// a barrier used for nothing else, then a bounded wait on it).
+__device__ __forceinline__ void drain_mmas(uint64_t* drain, long long limit, int32_t* status) {
+    mma_commit(drain);
+    if (!mbar_wait_quiet(smem_u32(drain), 0u, limit)) drain_failed(status);
 }
 
 __device__ __forceinline__ void tmem_fence_before() {
@@ -365,6 +405,7 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
         for (int b = 0; b < 2; b++) { mbar_init(&S.acc_full[b], 1); mbar_init(&S.acc_empty[b], 128); }
+        mbar_init(&S.drain, 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -379,21 +420,24 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const int nkb = static_cast<int>(G.H / kBK);
 
     if (warp == 0) {
-        if (lane == 0 && !G.withhold_loads) {                       // TMA producer
-            uint32_t it = 0;
+        if (lane == 0 && G.selftest != 1) {                         // TMA producer
+            uint32_t it = 0;                                        // stage loads issued
             for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
                 const TileCoords c = tile_coords(G, S.tile_prefix, t);
                 const int y_w = static_cast<int>(static_cast<int64_t>(c.e) * 2 * G.I) + kBN * c.nt;
                 for (int kb = 0; kb < nkb; kb++, it++) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1u, &S.abort, G.status, 1, G.wait_cycles)) goto done;
+                    if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1u, &S.abort, G.status, 1, G.wait_cycles))
+                        goto producer_end;
                     uint8_t* st = base + s * kStageBytes;
                     mbar_expect_tx(&S.full[s], kStageBytes);
                     tma_load_2d(st, &tmX, kb * kBK, static_cast<int>(c.row0), &S.full[s]);
                     tma_load_2d(st + kStageA, &tmW, kb * kBK, y_w, &S.full[s]);
                 }
             }
+        producer_end:
+            drain_loads(S.full, kStages, it, G.wait_cycles, G.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {                                            // MMA issuer
@@ -401,13 +445,14 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             for (int64_t t = blockIdx.x; t < total; t += gridDim.x, local++) {
                 const int b = static_cast<int>(local & 1u);
                 const uint32_t aph = (local >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&S.acc_empty[b]), aph ^ 1u, &S.abort, G.status, 2, G.wait_cycles)) goto done;
+                if (!mbar_wait(smem_u32(&S.acc_empty[b]), aph ^ 1u, &S.abort, G.status, 2, G.wait_cycles))
+                    goto issuer_end;
                 tmem_fence_after();
                 const uint32_t d_tmem = S.tmem_base + static_cast<uint32_t>(b * kBN);
                 for (int kb = 0; kb < nkb; kb++, it++) {
                     const int s = static_cast<int>(it % kStages);
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&S.full[s]), ph, &S.abort, G.status, 3, G.wait_cycles)) goto done;
+                    if (!mbar_wait(smem_u32(&S.full[s]), ph, &S.abort, G.status, 3, G.wait_cycles)) goto issuer_end;
                     tmem_fence_after();
                     const uint8_t* st = base + s * kStageBytes;
                     const uint64_t da = sw128_kmajor_desc(st), db = sw128_kmajor_desc(st + kStageA);
@@ -418,8 +463,10 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
                 }
                 mma_commit(&S.acc_full[b]);                         // accumulator complete
             }
+        issuer_end:
+            drain_mmas(&S.drain, G.wait_cycles, G.status);
         }
-    } else {                                                        // epilogue, warps 2-5
+    } else if (G.selftest != 2) {                                   // epilogue, warps 2-5
         const int quarter = warp & 3;
         const int trow = 32 * quarter + lane;
         uint32_t local = 0;
@@ -441,7 +488,6 @@ l1_gemm_swiglu_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             mbar_arrive(&S.acc_empty[b]);
         }
     }
-done:
     tmem_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -485,6 +531,7 @@ struct W4Shared {
     uint64_t bempty[kW4BStages];       // the MMA done with it
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
+    uint64_t drain;
     uint32_t tmem_base;
     int abort;
     int tile_prefix[kMaxGemmExperts + 1];
@@ -550,6 +597,7 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         }
         for (int j = 0; j < kW4BStages; j++) { mbar_init(&S.bready[j], kW4ConvThreads); mbar_init(&S.bempty[j], 1); }
         for (int b = 0; b < 2; b++) { mbar_init(&S.acc_full[b], 1); mbar_init(&S.acc_empty[b], 128); }
+        mbar_init(&S.drain, 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -564,15 +612,16 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int nkb = static_cast<int>(G.H / kBK);            // a multiple of 4 (H % 256 == 0)
 
     if (warp == 0) {
-        if (lane == 0 && !G.withhold_loads) {                       // TMA producer
-            uint32_t it = 0;
+        if (lane == 0 && G.selftest != 1) {                         // TMA producer
+            uint32_t it = 0;                                        // stage loads issued
             for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
                 const TileCoords c = tile_coords(G, S.tile_prefix, t);
                 const int y_w = static_cast<int>(static_cast<int64_t>(c.e) * 2 * G.I) + kBN * c.nt;
                 for (int kb = 0; kb < nkb; kb++, it++) {
                     const int s = static_cast<int>(it % kW4RawStages);
                     const uint32_t ph = (it / kW4RawStages) & 1u;
-                    if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1u, &S.abort, G.status, 1, G.wait_cycles)) goto done;
+                    if (!mbar_wait(smem_u32(&S.empty[s]), ph ^ 1u, &S.abort, G.status, 1, G.wait_cycles))
+                        goto producer_end;
                     uint8_t* st = base + s * kW4RawBytes;
                     const bool scales = (kb & 3) == 0;                // one scale tile per 4 stages
                     mbar_expect_tx(&S.full[s], kW4RawBytes + (scales ? kW4ScaleBytes : 0u));
@@ -583,6 +632,8 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                                     &S.full[s]);
                 }
             }
+        producer_end:
+            drain_loads(S.full, kW4RawStages, it, G.wait_cycles, G.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {                                            // MMA issuer
@@ -590,7 +641,8 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             for (int64_t t = blockIdx.x; t < total; t += gridDim.x, local++) {
                 const int b = static_cast<int>(local & 1u);
                 const uint32_t aph = (local >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&S.acc_empty[b]), aph ^ 1u, &S.abort, G.status, 2, G.wait_cycles)) goto done;
+                if (!mbar_wait(smem_u32(&S.acc_empty[b]), aph ^ 1u, &S.abort, G.status, 2, G.wait_cycles))
+                    goto issuer_end;
                 tmem_fence_after();
                 const uint32_t d_tmem = S.tmem_base + static_cast<uint32_t>(b * kBN);
                 for (int kb = 0; kb < nkb; kb++, it++) {
@@ -600,7 +652,7 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                                    G.wait_cycles) ||
                         !mbar_wait(smem_u32(&S.bready[j]), (it / kW4BStages) & 1u, &S.abort, G.status, 5,
                                    G.wait_cycles))
-                        goto done;
+                        goto issuer_end;
                     tmem_fence_after();
                     const uint64_t da = sw128_kmajor_desc(base + s * kW4RawBytes);
                     const uint64_t db = sw128_kmajor_desc(bconv + j * kStageB);
@@ -612,6 +664,8 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
                 }
                 mma_commit(&S.acc_full[b]);
             }
+        issuer_end:
+            drain_mmas(&S.drain, G.wait_cycles, G.status);
         }
     } else if (warp < 6) {                                          // epilogue, warps 2-5
         const int quarter = warp & 3;
@@ -657,7 +711,6 @@ l1_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             mbar_arrive(&S.empty[s]);
         }
     }
-done:
     tmem_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -756,7 +809,7 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I, float L,
                 const int32_t* offsets, int32_t E, int mode, uint8_t* packed, uint8_t* sf, void* out,
                 int32_t* status, cudaStream_t stream, long long wait_cycles = kWaitCycles,
-                int withhold_loads = 0) {
+                int selftest = 0) {
     if (rows < 0 || rows > (int64_t{1} << 31) - 2 * kBM) return MOE_NVFP4_ESIZE;
     if (H <= 0 || H % kBK != 0 || I <= 0 || I % (kBN / 2) != 0) return MOE_NVFP4_EWIDTH;
     const bool uses_L = mode == kOutNvfp4 || mode == kOutSwigluBf16;
@@ -782,11 +835,13 @@ int launch_gemm(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, 
     G.offsets = offsets; G.E = E; G.rows = rows; G.H = H; G.I = I;
     G.nt = static_cast<int>(2 * I / kBN); G.L = uses_L ? L : 1.0f;
     G.packed = packed; G.sf = sf; G.status = status;
-    G.wait_cycles = wait_cycles; G.withhold_loads = withhold_loads;
+    G.wait_cycles = wait_cycles; G.selftest = selftest;
     G.acc = mode == kOutAcc ? static_cast<float*>(out) : nullptr;
     G.out_bf16 = (mode == kOutGuBf16 || mode == kOutSwigluBf16) ? static_cast<uint16_t*>(out) : nullptr;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+    // the self-test that never releases an accumulator runs every tile on
+    // one CTA, so that its producer and MMA issuer have work in flight
+    cfg.gridDim = dim3(static_cast<unsigned>(selftest == 2 ? 1 : sms));
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = kGemmSmem;
     cfg.stream = stream;
@@ -838,7 +893,7 @@ int launch_gemm_w4(const uint16_t* x, const uint8_t* wq, const uint8_t* ws, int6
     G.offsets = offsets; G.E = E; G.rows = rows; G.H = H; G.I = I;
     G.nt = static_cast<int>(2 * I / kBN); G.L = mode == kOutNvfp4 ? L : 1.0f;
     G.packed = packed; G.sf = sf; G.acc = acc; G.out_bf16 = nullptr; G.status = status;
-    G.wait_cycles = kWaitCycles; G.withhold_loads = 0;
+    G.wait_cycles = kWaitCycles; G.selftest = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms));
     cfg.blockDim = dim3(kW4Threads);
@@ -875,11 +930,13 @@ int moe_l1_gemm_accumulators(const uint16_t* x, const uint16_t* w1, int64_t rows
 
 int moe_l1_gemm_wait_selftest(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,
                               const int32_t* expert_offsets, int32_t num_experts, uint8_t* packed,
-                              uint8_t* sf, int32_t* status, int64_t wait_cycles, moe_nvfp4_stream_t stream) {
+                              uint8_t* sf, int32_t* status, int64_t wait_cycles, int32_t mode,
+                              moe_nvfp4_stream_t stream) {
     if (status == nullptr) return MOE_NVFP4_ENULL;
     if (wait_cycles < 1000 || wait_cycles > kWaitCycles) return MOE_NVFP4_ESIZE;
+    if (mode != MOE_L1_GEMM_SELFTEST_NO_LOADS && mode != MOE_L1_GEMM_SELFTEST_NO_RELEASE) return MOE_NVFP4_EMODE;
     return launch_gemm(x, w1, rows, H, I, 7.0f, expert_offsets, num_experts, kOutNvfp4, packed, sf, nullptr,
-                       status, reinterpret_cast<cudaStream_t>(stream), wait_cycles, 1);
+                       status, reinterpret_cast<cudaStream_t>(stream), wait_cycles, mode);
 }
 
 int moe_l1_gemm_bf16(const uint16_t* x, const uint16_t* w1, int64_t rows, int64_t H, int64_t I,

@@ -167,10 +167,12 @@ def test_gemm_argument_errors(lib):
     assert b(A16, A16, 4, 64, 128, 7.0, A16, 1, 0, A2, NULL, S) == -3
     assert b(A16, A16, 0, 64, 128, 0.0, A16, 1, 0, NULL, NULL, S) == 0         # gu ignores L
     t = lib.moe_l1_gemm_wait_selftest
-    # (x, w1, rows, H, I, offsets, E, packed, sf, status, wait_cycles, stream)
-    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, NULL, 10 ** 7, S) == -1   # status required
-    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10, S) == -4         # limit out of range
-    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10 ** 12, S) == -4
+    # (x, w1, rows, H, I, offsets, E, packed, sf, status, wait_cycles, mode, stream)
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, NULL, 10 ** 7, 1, S) == -1   # status required
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10, 1, S) == -4         # limit out of range
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10 ** 12, 2, S) == -4
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10 ** 7, 0, S) == -9    # unknown mode
+    assert t(A16, A16, 4, 64, 128, A16, 1, A16, A16, A16, 10 ** 7, 3, S) == -9
     w4 = lib.moe_l1_gemm_w4_swiglu_nvfp4
     # (x, w1_packed, w1_sf, rows, H, I, clamp_L, offsets, E, packed, sf, status, stream)
     assert w4(A16, A16, A16, 4, 128, 128, 7.0, A16, 1, A16, A16, NULL, S) == -2   # H % 256

@@ -3,7 +3,8 @@ check (non-monotone, out-of-range and overlapping padded offsets set their
 status bits; valid ones set none), the traffic-floor kernels (they touch
 every block: their stores are the XOR of the words each block read), and the
 fused and quantize-only steps on both sides of the size where the launch
-shape changes from one block per thread to the persistent grid."""
+shape changes from the small-problem kernels to the persistent grid, and
+the small fused kernel's exact paths on near-tie blocks."""
 import numpy as np
 import pytest
 import torch
@@ -104,7 +105,10 @@ def test_traffic_floor_touches_every_block(kind, rows, width):
     a, b = xor_fold_blocks(src, 16 if kind == "fused" else 8)
     got = packed.cpu().numpy().reshape(-1, 8).view(np.uint32)
     assert np.array_equal(got[:, 0], a) and np.array_equal(got[:, 1], b)
-    assert np.array_equal(sf.cpu().numpy().ravel(), ((a ^ b) & 0xFF).astype(np.uint8))
+    # the scale byte is a byte of the folded words (the persistent shape
+    # folds both halves, the small fused shape's even lane its own)
+    g = sf.cpu().numpy().ravel()
+    assert np.all((g == ((a ^ b) & 0xFF)) | (g == (a & 0xFF)))
 
 
 def test_traffic_floor_read_sweep_and_empty_launch():
@@ -119,13 +123,16 @@ def test_traffic_floor_read_sweep_and_empty_launch():
 
 
 def _shape_boundary_rows(width: int) -> list:
-    """Row counts whose block count sits at the largest size the one-block-
-    per-thread shape takes (152 SMs x 3 CTAs x 256 threads) and just past
-    it, where the persistent grid takes over."""
+    """Row counts whose block counts span the sizes where the launch shape
+    changes from the small-problem kernels (one block per thread for
+    quantize-only, two threads per block for the fused step, up to one wave
+    of their resident CTAs: about 0.7 to 1.2 x 10^5 blocks on 152 SMs,
+    depending on their register counts) to the persistent grid, plus a
+    ragged tail at each."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    cap = sms * 3 * 256
     bpr = width // 16
-    return sorted({cap // bpr, cap // bpr + 1, (cap + bpr - 1) // bpr + 7})
+    blocks = [sms * 128 * k // 2 for k in (7, 8, 10, 12)] + [sms * 128 * k for k in (5, 6, 7, 8)]
+    return sorted({b // bpr + d for b in blocks for d in (0, 1)})
 
 
 @pytest.mark.parametrize("I", [2048, 3072])
@@ -151,8 +158,9 @@ def test_quantize_on_both_sides_of_the_launch_shape_boundary():
 
 
 def test_small_shape_ragged_offsets_with_sentinels():
-    """One block per thread with device offsets: rows outside the segments
-    keep their contents, including when the segments start past row 0."""
+    """The small-problem shape with device offsets: rows outside the
+    segments keep their contents, including when the segments start past
+    row 0."""
     w = W.ragged_routing(tokens=128, experts=16, topk=4, I=1024, pad_rows=33)
     off = w.offsets.astype(np.int64) + 17
     off = np.minimum(off, w.rows).astype(np.int32)
@@ -164,3 +172,25 @@ def test_small_shape_ragged_offsets_with_sentinels():
     torch.cuda.synchronize()
     rp, rs = oracle.swiglu_quantize_nvfp4(w.data, w.clamp_L, off, packed=sent_p, sf=sent_s)
     assert np.array_equal(p.cpu().numpy(), rp) and np.array_equal(s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("n_blocks,I", [(2048, 2048), (4096, 512)])
+def test_small_shape_near_tie_blocks_exact(n_blocks, I):
+    """Near-tie blocks (amax on 6 x E4M3 values and on 6 x midpoints, other
+    outputs on half-step ties) at a size the small-problem kernel takes:
+    both of its re-evaluation paths (the scale, shared by the two lanes of a
+    block, and the nibbles) must give the definition's bytes."""
+    rng = np.random.default_rng(n_blocks + I)
+    blocks, stats = parity.fused_near_tie_blocks(rng, n_blocks, 7.0)
+    gu = blocks.reshape(-1, 2 * I)
+    gp, gs = M.moe_swiglu_nvfp4_quantize(torch.from_numpy(gu.view(np.int16)).cuda(), 7.0)
+    cnt = torch.zeros(3, dtype=torch.int64, device="cuda")
+    M.moe_swiglu_nvfp4_quantize_counted(torch.from_numpy(gu.view(np.int16)).cuda(), 7.0, cnt)
+    torch.cuda.synchronize()
+    rp, rs = oracle.swiglu_quantize_nvfp4(gu, 7.0)
+    rep = parity.compare_fused(gp.cpu().numpy(), gs.cpu().numpy(), rp, rs,
+                               lambda r, c: float(oracle.swiglu_values(gu, 7.0, r, r + 1)[0, c]))
+    rep.assert_within_tolerance()
+    assert rep.exact, rep
+    blocks_done, scales, nibbles = (int(v) for v in cnt.cpu())
+    assert blocks_done == n_blocks and scales > 0 and nibbles > 0      # both paths ran (counted variant)

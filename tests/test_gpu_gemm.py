@@ -196,7 +196,7 @@ def test_expired_wait_reports_its_status_and_the_device_stays_usable():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     sp = torch.full((w.rows, w.I // 2), 0xA5, dtype=torch.uint8, device="cuda")
     ss = torch.full((w.rows, w.I // 16), 0x5A, dtype=torch.uint8, device="cuda")
-    M.moe_l1_gemm_wait_selftest(x, w1, off, status, 20_000_000, sp, ss)
+    M.moe_l1_gemm_wait_selftest(x, w1, off, status, 20_000_000, sp, ss, mode="no_loads")
     code = int(host(status)[0])
     assert code in (3, 4), code
     assert bool((sp == 0xA5).all()) and bool((ss == 0x5A).all())
@@ -270,3 +270,28 @@ def test_w4_gemm_full_width():
     ref = oracle.l1_gemm_accumulators(w.x[rows], deq, sub_off)
     mag = oracle.l1_gemm_abs_accumulators(w.x[rows], deq, sub_off)
     assert np.all(np.abs(a4[rows] - ref) <= acc_bound(H) * mag + 1e-30)
+
+
+def test_expired_wait_with_work_in_flight_drains_before_exit():
+    """The abort path with loads and MMAs issued: the epilogue never frees
+    an accumulator, and one CTA runs every tile, so after two tiles the MMA
+    issuer's wait (or the producer's, for a stage of the third) expires
+    while TMA loads for the next tile and the MMAs of the first two were
+    issued. Both roles wait for that work before the TMEM is released: the
+    status holds the expired wait's code (never the drain's 8), the outputs
+    stay untouched, and the next GEMM on the device is correct."""
+    w = _case("ragged_pad")
+    x, w1, off = dev(w.x), dev(w.w1), torch.from_numpy(w.offsets).cuda()
+    assert w.active_rows // 128 * (2 * w.I // 256) >= 3                   # at least three tiles
+    for _ in range(2):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sp = torch.full((w.rows, w.I // 2), 0xA5, dtype=torch.uint8, device="cuda")
+        ss = torch.full((w.rows, w.I // 16), 0x5A, dtype=torch.uint8, device="cuda")
+        M.moe_l1_gemm_wait_selftest(x, w1, off, status, 20_000_000, sp, ss, mode="no_release")
+        code = int(host(status)[0])
+        assert code in (1, 2), code
+        assert bool((sp == 0xA5).all()) and bool((ss == 0x5A).all())
+    p, s, acc = _run(w)
+    r0, r1 = int(w.offsets[0]), int(w.offsets[-1])
+    y_ref = oracle.gemm_swiglu_values(acc[r0:r1].astype(np.float64), w.clamp_L)
+    parity.compare_gemm_fused(p[r0:r1], s[r0:r1], y_ref)
