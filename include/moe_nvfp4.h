@@ -158,7 +158,10 @@ MOE_NVFP4_API int moe_nvfp4_quantize_scaled(const uint16_t *x, int64_t rows, int
                                             moe_nvfp4_stream_t stream);
 
 /* The fused step with options (NULL = the plain step). With out_offsets,
- * packed and sf have out_rows rows and num_experts must be > 0. */
+ * packed and sf have out_rows rows and num_experts must be > 0.
+ * MOE_NVFP4_ESIZE also for rows * I / 16 >= 2^32 (256 GiB of input or more,
+ * beyond one device's memory with the outputs); the same for
+ * moe_swiglu_bf16. */
 MOE_NVFP4_API int moe_swiglu_nvfp4_quantize_ex(const uint16_t *gu, int64_t rows, int64_t I,
                                                float clamp_L, const int32_t *expert_offsets,
                                                int32_t num_experts,

@@ -642,20 +642,34 @@ __device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool val
         const uint32_t t = static_cast<uint32_t>(ceilf(1.5f * e)) + 2u;
         tol = t < tol ? t : tol;
     }
-    // ((bits + tol - 0x8000) mod 2^16) <= 2 tol, computed in the top half
-    const uint32_t c16 = (tol - 0x8000u) << 16, t16 = ((2u * tol) << 16) | 0xFFFFu;
-    uint32_t amb = 0;
+    // A value is near a midpoint when ((bits + tol - 0x8000) mod 2^16) <= 2
+    // tol. Block test first, two values per word: the low halves of a pair
+    // side by side, tol + 0x8000 added to both halves by one 32-bit add (a
+    // carry out of the low half raises the high half by one, so both are
+    // held to 2 tol + 1: false alarms only), and the least half over the
+    // block by min.u16x2. Element by element only when it fires.
+    const uint32_t both = (tol + 0x8000u) * 0x10001u;
+    uint32_t least = 0xFFFFFFFFu;
 #pragma unroll
     for (int q = 0; q < 8; q++) {
         yb[q] = bf16x2_rn(y[2 * q + 1], y[2 * q]);
-        amb |= (near_bf16_midpoint(y[2 * q], c16, t16) << (2 * q)) |
-               (near_bf16_midpoint(y[2 * q + 1], c16, t16) << (2 * q + 1));
+        least = u16x2_min(least, __byte_perm(__float_as_uint(y[2 * q]), __float_as_uint(y[2 * q + 1]), 0x5410) + both);
+    }
+    uint32_t amb = 0;
+    if ((least & 0xFFFFu) <= 2u * tol + 1u || (least >> 16) <= 2u * tol + 1u) {
+        // the test in the top half of the word: one multiply-add and a compare
+        const uint32_t c16 = (tol - 0x8000u) << 16, t16 = ((2u * tol) << 16) | 0xFFFFu;
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            amb |= (near_bf16_midpoint(y[2 * q], c16, t16) << (2 * q)) |
+                   (near_bf16_midpoint(y[2 * q + 1], c16, t16) << (2 * q + 1));
     }
     // block pre-test for the window's range (gates below the floor, results
     // near underflow); element by element only when it fires
     float ymin = fabsf(y[0]);
 #pragma unroll
-    for (int i = 1; i < 16; i++) ymin = fminf(ymin, fabsf(y[i]));
+    for (int i = 1; i < 15; i += 2) ymin = min3(ymin, fabsf(y[i]), fabsf(y[i + 1]));
+    ymin = fminf(ymin, fabsf(y[15]));
     if (gmin < X.gate_floor || ymin < 0x1p-100f) {
 #pragma unroll
         for (int i = 0; i < 16; i++) {
@@ -812,6 +826,109 @@ swiglu_ex_kernel(const ExArgs X) {
         pad_e[threadIdx.x] = -1;
     }
     __syncthreads();
+    // the compat modes without padded output: each warp's queue of blocks
+    // with an element to re-evaluate (at most 31 left plus 32 kUnroll from
+    // one chunk), as offsets from cta_begin (the launcher admits fewer than
+    // 2^32 blocks in all). The
+    // compact writer resolves in place: it streams near the copy floor, where
+    // each warp's last pass over its queue lengthens the launch more than
+    // the queue saves on data with few undecided elements.
+    constexpr bool kDefer = (kMode == kExCompat || kMode == kExCompatUnit) && !kPadded;
+    constexpr int kQueue = 31 + 32 * kUnroll;
+    __shared__ uint32_t defer_q[kDefer ? kThreads / 32 : 1][kDefer ? kQueue : 1];
+    int deferred = 0;                                        // warp-uniform
+    // output block of block blk: its padded position and whether it is
+    // stored (called by the whole warp after the block's arithmetic)
+    auto out_block = [&](int64_t blk, bool valid, int64_t& oblk, bool& store) {
+        oblk = blk;
+        store = valid;
+        if (!padded) return;
+        PadSegment sg = pad_seg[threadIdx.x];
+        if (valid && blk >= sg.end_blk) {               // once per segment
+            // a thread's blocks only move forward: step on from its
+            // segment, else bisect
+            int e = pad_e[threadIdx.x];
+            const int64_t row = blk / A.bpr;
+            for (int t = 0; e >= 0 && t < 4 && e + 1 < A.E && row >= __ldg(A.offsets + e + 1); t++)
+                e++;
+            if (e < 0 || (e + 1 < A.E && row >= __ldg(A.offsets + e + 1)))
+                e = segment_of(A.offsets, A.E, row);
+            // rows are int32, so the stored-row range is clamped to [0, 2^31]
+            const int64_t shift = static_cast<int64_t>(__ldg(X.out_offsets + e)) - __ldg(A.offsets + e);
+            const int64_t lo = -shift, hi = X.out_rows - shift, top = int64_t(1) << 31;
+            sg.end_blk = static_cast<int64_t>(__ldg(A.offsets + e + 1)) * A.bpr;
+            sg.lo_blk = (lo < 0 ? 0 : (lo > top ? top : lo)) * A.bpr;
+            sg.hi_blk = (hi < 0 ? 0 : (hi > top ? top : hi)) * A.bpr;
+            sg.shift_blk = shift * A.bpr;
+            pad_seg[threadIdx.x] = sg;
+            pad_e[threadIdx.x] = e;
+        }
+        store = valid && blk >= sg.lo_blk && blk < sg.hi_blk;
+        oblk = blk + sg.shift_blk;
+    };
+    // the end of a BF16-mode block: the compact writer stores its BF16
+    // values; the compat mode quantizes them (and stores where out_block says)
+    auto finish_block = [&](int64_t blk, bool valid, const uint32_t* b) {
+        if (kMode == kExCompact) {
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(X.out_bf16 + blk * 16);
+                dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+                dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
+            }
+            return;
+        }
+        float v[16];
+        uint32_t lo, hi, code;
+        if (kMode == kExCompatUnit) {                       // BF16 values: the cheap exact form
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                v[2 * q] = bf16_lo(b[q]);
+                v[2 * q + 1] = bf16_hi(b[q]);
+            }
+            code = quantize16_exact<false, true>(v, lo, hi);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const float2 vv = __fmul2_rn(make_float2(bf16_lo(b[q]), bf16_hi(b[q])), make_float2(X.gs, X.gs));
+                v[2 * q] = vv.x;
+                v[2 * q + 1] = vv.y;
+            }
+            code = quantize16_exact<true, true>(v, lo, hi);
+        }
+        int64_t oblk;
+        bool store;
+        out_block(blk, valid, oblk, store);
+        if (store) {
+            *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
+            A.sf[oblk] = static_cast<uint8_t>(code);
+        }
+    };
+    // the warp's queued blocks (n, warp-uniform), one per lane per pass:
+    // reloaded (still in L2), recomputed, their undecided elements
+    // re-evaluated by the definition, then finished
+    auto finish_deferred = [&](int n) {
+        __syncwarp();
+        const uint32_t* q = defer_q[threadIdx.x >> 5];
+        for (int p0 = 0; p0 < n; p0 += 32) {
+            const bool have = p0 + lane < n;
+            const int64_t blk = have ? cta_begin + q[p0 + lane] : 0;
+            uint32_t w1[16];
+            if (have) {
+                load_nc_32B(A.gu + blk * 32, w1);
+                load_nc_32B(A.gu + blk * 32 + 16, w1 + 8);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) w1[j] = 0u;
+            }
+            float y[16];
+            fast_swiglu16<kBf16Clamp>(A, w1, y);
+            uint32_t b[8];
+            const uint32_t m = bf16_fast_of_block(X, have, w1, y, b);
+            resolve_bf16_elements<16>(A, blk, m, b);
+            if (have) finish_block(blk, true, b);
+        }
+        __syncwarp();
+    };
     for (;;) {                                              // warp-uniform
         int c = 0;
         if (lane == 0) c = atomicAdd(&next_chunk, 1);
@@ -839,35 +956,6 @@ swiglu_ex_kernel(const ExArgs X) {
                 for (int j = 0; j < 16; j++) w[k][j] = 0u;
             }
         }
-        // output block of block blk: its padded position and whether it is
-        // stored (called by the whole warp after the block's arithmetic)
-        auto out_block = [&](int64_t blk, bool valid, int64_t& oblk, bool& store) {
-            oblk = blk;
-            store = valid;
-            if (!padded) return;
-            PadSegment sg = pad_seg[threadIdx.x];
-            if (valid && blk >= sg.end_blk) {               // once per segment
-                // a thread's blocks only move forward: step on from its
-                // segment, else bisect
-                int e = pad_e[threadIdx.x];
-                const int64_t row = blk / A.bpr;
-                for (int t = 0; e >= 0 && t < 4 && e + 1 < A.E && row >= __ldg(A.offsets + e + 1); t++)
-                    e++;
-                if (e < 0 || (e + 1 < A.E && row >= __ldg(A.offsets + e + 1)))
-                    e = segment_of(A.offsets, A.E, row);
-                // rows are int32, so the stored-row range is clamped to [0, 2^31]
-                const int64_t shift = static_cast<int64_t>(__ldg(X.out_offsets + e)) - __ldg(A.offsets + e);
-                const int64_t lo = -shift, hi = X.out_rows - shift, top = int64_t(1) << 31;
-                sg.end_blk = static_cast<int64_t>(__ldg(A.offsets + e + 1)) * A.bpr;
-                sg.lo_blk = (lo < 0 ? 0 : (lo > top ? top : lo)) * A.bpr;
-                sg.hi_blk = (hi < 0 ? 0 : (hi > top ? top : hi)) * A.bpr;
-                sg.shift_blk = shift * A.bpr;
-                pad_seg[threadIdx.x] = sg;
-                pad_e[threadIdx.x] = e;
-            }
-            store = valid && blk >= sg.lo_blk && blk < sg.hi_blk;
-            oblk = blk + sg.shift_blk;
-        };
         if (kMode == kExQuantize) {
 #pragma unroll
             for (int k = 0; k < kUnroll; k++) {
@@ -886,8 +974,9 @@ swiglu_ex_kernel(const ExArgs X) {
                 }
             }
         } else {
-            // BF16 values: fast pass over all blocks, one joint re-evaluation
-            // of the undecided pairs, then store or quantize
+            // BF16 values: fast pass over all blocks; blocks with an element
+            // whose BF16 rounding the fast value cannot decide are finished
+            // later (below), then store or quantize
             uint32_t yb[8 * kUnroll];
             uint32_t elems = 0;
 #pragma unroll
@@ -897,48 +986,39 @@ swiglu_ex_kernel(const ExArgs X) {
                 elems |= bf16_fast_of_block(X, base + 32 * k + lane < cta_end, w[k], y, yb + 8 * k)
                          << (16 * k);
             }
-            resolve_bf16_elements<16 * kUnroll>(A, base + lane, elems, yb);
+            if constexpr (!kDefer) {
+                // resolved here: padded output keeps each thread's blocks in
+                // order (its segment cache moves forward only); the compact
+                // writer is faster this way on typical data
+                resolve_bf16_elements<16 * kUnroll>(A, base + lane, elems, yb);
+            } else if (__any_sync(kFullMask, elems != 0u)) {
+                // rare (about one block in 130): queued for the warp, which
+                // finishes them 32 at a time, one block per lane, instead of
+                // one element per pass while the other lanes wait
+                uint32_t* q = defer_q[threadIdx.x >> 5];
+                const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+                for (int k = 0; k < kUnroll; k++) {
+                    const bool f = ((elems >> (16 * k)) & 0xFFFFu) != 0u;
+                    const unsigned bal = __ballot_sync(kFullMask, f);
+                    if (f) q[deferred + __popc(bal & below)] = static_cast<uint32_t>(base + 32 * k + lane - cta_begin);
+                    deferred += __popc(bal);
+                }
+                if (deferred >= 32) {
+                    finish_deferred(deferred);
+                    deferred = 0;
+                }
+            }
 #pragma unroll
             for (int k = 0; k < kUnroll; k++) {
                 const int64_t blk = base + 32 * k + lane;
-                const bool valid = blk < cta_end;
-                const uint32_t* b = yb + 8 * k;
-                if (kMode == kExCompact) {
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(X.out_bf16 + blk * 16);
-                        dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
-                        dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
-                    }
-                } else {                                // compat: quantize the BF16 values
-                    float v[16];
-                    uint32_t lo, hi, code;
-                    if (kMode == kExCompatUnit) {               // BF16 values: the cheap exact form
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            v[2 * q] = bf16_lo(b[q]);
-                            v[2 * q + 1] = bf16_hi(b[q]);
-                        }
-                        code = quantize16_exact<false, true>(v, lo, hi);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            const float2 vv = __fmul2_rn(make_float2(bf16_lo(b[q]), bf16_hi(b[q])),
-                                                         make_float2(X.gs, X.gs));
-                            v[2 * q] = vv.x;
-                            v[2 * q + 1] = vv.y;
-                        }
-                        code = quantize16_exact<true, true>(v, lo, hi);
-                    }
-                    int64_t oblk;
-                    bool store;
-                    out_block(blk, valid, oblk, store);
-                    if (store) {
-                        *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
-                        A.sf[oblk] = static_cast<uint8_t>(code);
-                    }
-                }
+                if (kDefer && ((elems >> (16 * k)) & 0xFFFFu) != 0u) continue;       // queued
+                finish_block(blk, blk < cta_end, yb + 8 * k);
             }
         }
+    }
+    if constexpr (kDefer) {
+        if (deferred > 0) finish_deferred(deferred);
     }
 }
 
@@ -1580,6 +1660,9 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     if ((E > 0 && !aligned(offsets, 4)) || (out_offsets != nullptr && !aligned(out_offsets, 4)))
         return MOE_NVFP4_EALIGN;
     if (rows == 0) return MOE_NVFP4_OK;
+    // the compat modes queue blocks by a 32-bit offset inside a CTA's range
+    // (2^32 blocks are 256 GiB of input, beyond one device with its outputs)
+    if (rows * (I / 16) >= (int64_t(1) << 32)) return MOE_NVFP4_ESIZE;
     DeviceInfo di;
     if ((rc = device_info(di)) != MOE_NVFP4_OK) return rc;
     // BF16 roundings compare the fast value itself: W |y| <= W 2^24 ulps,

@@ -87,6 +87,19 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Per 16-bit half, the smaller unsigned value.
+__device__ __forceinline__ uint32_t u16x2_min(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

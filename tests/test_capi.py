@@ -124,9 +124,14 @@ def test_extension_argument_errors(lib):
     assert ex(A32, 4, 32, 7.0, A2, 2, None, A16, A16, S) == -3     # offsets 4-byte aligned
     bad_out = FusedOptions(1.0, 0, A2.value, 8)
     assert ex(A32, 4, 32, 7.0, A16, 2, C.byref(bad_out), A16, A16, S) == -3
+    compat = FusedOptions(1.0, 1, None, 0)
+    # 2^32 blocks (256 GiB of input) and more are refused before any device call
+    assert ex(A32, 1 << 28, 256, 7.0, NULL, 0, C.byref(compat), A16, A16, S) == -4
+    assert ex(A32, 1 << 24, 1 << 16, 7.0, NULL, 0, C.byref(compat), A16, A16, S) == -4
     cw = lib.moe_swiglu_bf16
     assert cw(A32, 4, 32, 7.0, NULL, 0, NULL, S) == -1
     assert cw(A32, 4, 32, 7.0, NULL, 0, A2, S) == -3
+    assert cw(A32, 1 << 28, 256, 7.0, NULL, 0, A32, S) == -4
     dq = lib.moe_nvfp4_dequantize
     assert dq(A16, A16, 4, 24, 1.0, A32, S) == -2
     assert dq(A16, A16, 4, 32, 0.0, A32, S) == -8
