@@ -222,6 +222,35 @@ def test_compact_writer_and_compat_near_bf16_midpoints():
         assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp)
 
 
+def test_compact_writer_and_compat_results_near_underflow():
+    """Results below 2^-100 (tiny and subnormal BF16 ups or gates): whole
+    blocks of them, and a few of them beside normal results. The compat
+    modes do not re-decide them up to a global scale of 2^86 (they cannot
+    change a byte there); the compact writer does, and so does compat above
+    2^86, where a global scale of 2^110 brings them up to values that
+    matter."""
+    rng = np.random.default_rng(93)
+    nblk = 512
+    g = rng.normal(0.0, 2.0, (nblk, 16)).astype(np.float32)
+    u = rng.normal(0.0, 1.0, (nblk, 16)).astype(np.float32)
+    tiny = np.ldexp(rng.uniform(1.0, 2.0, (nblk, 16)), rng.integers(-133, -100, (nblk, 16))).astype(np.float32)
+    tiny *= np.where(rng.random((nblk, 16)) < 0.5, -1.0, 1.0).astype(np.float32)
+    kind = np.arange(nblk) % 4
+    u = np.where((kind == 0)[:, None], tiny, u)                         # whole blocks tiny
+    few = (kind == 1)[:, None] & (rng.random((nblk, 16)) < 0.8)
+    u = np.where(few, tiny, u)                                          # tiny beside normal
+    g = np.where(((kind == 2)[:, None]) & (rng.random((nblk, 16)) < 0.5), tiny, g)   # tiny gates
+    gb = W.bf16_bits(g)
+    ub = W.bf16_bits(u)
+    gu = W.interleave_gate_up(gb, ub).reshape(-1, 8 * 32)
+    out = M.moe_swiglu_bf16(dev(gu), 7.0)
+    assert np.array_equal(bits(out), oracle.swiglu_bf16(gu, 7.0))
+    for gs in (1.0, 1.7, 2.0 ** 86, 2.0 ** 110):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(gu), 7.0, global_scale=gs, round_to_bf16=True)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(gu, 7.0, global_scale=gs, round_bf16=True)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), gs
+
+
 def test_compact_writer_and_compat_near_bf16_midpoints_negative_gates():
     """The per-block tolerance grows with the most negative gate; here every
     gate is in [-16, -4] and every output sits next to a BF16 midpoint."""
