@@ -921,30 +921,32 @@ swiglu_ex_kernel(const ExArgs X) {
             A.sf[oblk] = static_cast<uint8_t>(code);
         }
     };
-    // the warp's queued blocks (n, warp-uniform), one per lane per pass:
-    // reloaded (still in L2), recomputed, their undecided elements
-    // re-evaluated by the definition, then finished
+    // one pass over up to 32 queued blocks, one per lane (have: this lane
+    // has one, block blk; a warp-uniform call): reloaded (still in L2),
+    // recomputed, the undecided elements re-evaluated by the definition,
+    // then finished
+    auto finish_pass = [&](bool have, int64_t blk) {
+        uint32_t w1[16];
+        if (have) {
+            load_nc_32B(A.gu + blk * 32, w1);
+            load_nc_32B(A.gu + blk * 32 + 16, w1 + 8);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; j++) w1[j] = 0u;
+        }
+        float y[16];
+        fast_swiglu16<kBf16Clamp>(A, w1, y);
+        uint32_t b[8];
+        const uint32_t m = bf16_fast_of_block<kTinyTest>(X, have, w1, y, b);
+        resolve_bf16_elements<16>(A, blk, m, b);
+        if (have) finish_block(blk, true, b);
+    };
+    // the warp's n queued blocks (n warp-uniform), 32 per pass
     auto finish_deferred = [&](int n) {
         __syncwarp();
         const uint32_t* q = defer_q[threadIdx.x >> 5];
-        for (int p0 = 0; p0 < n; p0 += 32) {
-            const bool have = p0 + lane < n;
-            const int64_t blk = have ? cta_begin + q[p0 + lane] : 0;
-            uint32_t w1[16];
-            if (have) {
-                load_nc_32B(A.gu + blk * 32, w1);
-                load_nc_32B(A.gu + blk * 32 + 16, w1 + 8);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; j++) w1[j] = 0u;
-            }
-            float y[16];
-            fast_swiglu16<kBf16Clamp>(A, w1, y);
-            uint32_t b[8];
-            const uint32_t m = bf16_fast_of_block<kTinyTest>(X, have, w1, y, b);
-            resolve_bf16_elements<16>(A, blk, m, b);
-            if (have) finish_block(blk, true, b);
-        }
+        for (int p0 = 0; p0 < n; p0 += 32)
+            finish_pass(p0 + lane < n, p0 + lane < n ? cta_begin + q[p0 + lane] : 0);
         __syncwarp();
     };
     for (;;) {                                              // warp-uniform
@@ -1037,7 +1039,26 @@ swiglu_ex_kernel(const ExArgs X) {
         }
     }
     if constexpr (kDefer) {
-        if (deferred > 0) finish_deferred(deferred);
+        // the CTA's leftover queues (each under 32 blocks), concatenated in
+        // warp order: warp w finishes entries [32 w, 32 w + 32), so the CTA
+        // runs as many passes as its leftovers need instead of one per warp
+        __shared__ int defer_n[kThreads / 32];
+        const int warp = threadIdx.x >> 5;
+        if (lane == 0) defer_n[warp] = deferred;
+        __syncthreads();
+        const int i = 32 * warp + lane;
+        int total = 0, owner = -1, pos = 0;
+#pragma unroll
+        for (int v = 0; v < kThreads / 32; v++) {
+            const int c = defer_n[v];
+            if (i >= total && i < total + c) {
+                owner = v;
+                pos = i - total;
+            }
+            total += c;
+        }
+        if (32 * warp < total)                                 // warp-uniform
+            finish_pass(owner >= 0, owner >= 0 ? cta_begin + defer_q[owner][pos] : 0);
     }
 }
 
