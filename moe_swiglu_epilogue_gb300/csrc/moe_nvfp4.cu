@@ -258,8 +258,8 @@ struct FusedArgs {
     float* values;             // [rows, I] (fast-values variant)
 };
 
-struct Tally {
-    unsigned long long blocks = 0, scales = 0, nibbles = 0;
+struct Tally {                  // one thread's counts (far below 2^32: its blocks are at most its CTA's / 32)
+    uint32_t blocks = 0, scales = 0, nibbles = 0;
 };
 
 __device__ __forceinline__ void active_block_range(const int32_t* offsets, int E, int64_t rows,
@@ -457,25 +457,6 @@ __device__ __noinline__ void resolve_chunk(const uint16_t* gu, uint8_t* packed, 
         [&](int owner, int k, int i, uint32_t nib, int64_t) { patch_nibble(packed + (base + 32 * k + owner) * 8, i, nib); });
 }
 
-// The fused step for one chunk of a warp: kUnroll blocks per lane at
-// blk0 + 32 k (k < kUnroll), loaded in w; then one warp-wide re-decision of
-// every element left to the definition in the chunk. Every lane calls this
-// together.
-template <bool kCount, bool kBf16Clamp>
-__device__ __forceinline__ void fused_chunk(const FusedArgs& A, int64_t blk0, int64_t end, int lane,
-                                            const uint32_t (*w)[16], Tally& tally) {
-    static_assert(kUnroll * 16 <= 32 && kUnroll * 8 <= 32, "element bits and codes fit a word");
-    uint32_t mask = 0, codes = 0;
-#pragma unroll
-    for (int k = 0; k < kUnroll; k++) {
-        uint32_t code;
-        mask |= fused_block<kCount, kBf16Clamp>(A, blk0 + 32 * k, blk0 + 32 * k < end, w[k], code, tally)
-                << (16 * k);
-        codes |= code << (8 * k);
-    }
-    if (__any_sync(kFullMask, mask != 0u)) resolve_chunk(A.gu, A.packed, A.L, blk0 - lane, lane, mask, codes);
-}
-
 // The diagnostic variant: the fast fp32 values of one block, in output
 // column order.
 template <bool kBf16Clamp>
@@ -501,7 +482,7 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
     // Each CTA owns an equal contiguous range of blocks; its warps claim
     // chunks of 32 * kUnroll blocks from a shared counter, so a warp held up
     // by exact re-evaluations (or slow memory) takes fewer chunks and the
-    // CTA's other warps absorb the delay.
+    // CTA's other warps absorb the delay. A chunk is two blocks per lane.
     constexpr int64_t kChunk = 32 * kUnroll;
     const int64_t total = b1 - b0;
     int64_t per_cta = (total + gridDim.x - 1) / gridDim.x;
@@ -511,38 +492,59 @@ swiglu_nvfp4_kernel(const FusedArgs A) {
     __shared__ int next_chunk;
     if (threadIdx.x == 0) next_chunk = 0;
     __syncthreads();
-    Tally tally;
-    for (;;) {                                              // warp-uniform
+    static_assert(kUnroll == 2, "two blocks per lane per chunk");
+    auto claim = [&]() {                                    // warp-uniform
         int c = 0;
         if (lane == 0) c = atomicAdd(&next_chunk, 1);
         c = __shfl_sync(kFullMask, c, 0);
-        const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
-        if (base >= cta_end) break;
-        uint32_t w[kUnroll][16];
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + 32 * k + lane;
-            if (blk < cta_end) {
-                const uint16_t* p = A.gu + blk * 32;
-                load_stream_32B(p, pol, w[k]);
-                load_stream_32B(p + 16, pol, w[k] + 8);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; j++) w[k][j] = 0u;
-            }
-        }
-        if (kValues) {
-#pragma unroll
-            for (int k = 0; k < kUnroll; k++)
-                fast_values_block<kBf16Clamp>(A, base + 32 * k + lane, base + 32 * k + lane < cta_end, w[k]);
+        return cta_begin + static_cast<int64_t>(c) * kChunk;
+    };
+    auto load_block = [&](int64_t blk, uint32_t* w) {
+        if (blk < cta_end) {
+            const uint16_t* p = A.gu + blk * 32;
+            load_stream_32B(p, pol, w);
+            load_stream_32B(p + 16, pol, w + 8);
         } else {
-            fused_chunk<kCount, kBf16Clamp>(A, base + lane, cta_end, lane, w, tally);
+#pragma unroll
+            for (int j = 0; j < 16; j++) w[j] = 0u;
         }
+    };
+    Tally tally;
+    // Software pipeline over the lane's blocks, one block ahead: while a
+    // block is computed, the next one's loads are in flight (the second
+    // block of the chunk, then the first block of the next chunk, claimed
+    // early), so a warp never computes with none of its own loads pending.
+    // Then one warp-wide re-decision of every element of the chunk left to
+    // the definition.
+    uint32_t w0[16], w1[16];
+    int64_t base = claim();
+    load_block(base + lane, w0);
+    while (base < cta_end) {                                // warp-uniform
+        load_block(base + 32 + lane, w1);
+        if (kValues) {
+            fast_values_block<kBf16Clamp>(A, base + lane, base + lane < cta_end, w0);
+            const int64_t next = claim();
+            load_block(next + lane, w0);
+            fast_values_block<kBf16Clamp>(A, base + 32 + lane, base + 32 + lane < cta_end, w1);
+            base = next;
+            continue;
+        }
+        uint32_t code0, code1;
+        const uint32_t m0 =
+            fused_block<kCount, kBf16Clamp>(A, base + lane, base + lane < cta_end, w0, code0, tally);
+        const int64_t next = claim();
+        load_block(next + lane, w0);
+        const uint32_t m1 =
+            fused_block<kCount, kBf16Clamp>(A, base + 32 + lane, base + 32 + lane < cta_end, w1, code1, tally);
+        const uint32_t mask = m0 | (m1 << 16);
+        if (__any_sync(kFullMask, mask != 0u))
+            resolve_chunk(A.gu, A.packed, A.L, base, lane, mask, code0 | (code1 << 8));
+        base = next;
     }
     if (kCount) {
-        atomicAdd(A.counters + 0, tally.blocks);
-        if (tally.scales) atomicAdd(A.counters + 1, tally.scales);
-        if (tally.nibbles) atomicAdd(A.counters + 2, tally.nibbles);
+        atomicAdd(A.counters + 0, static_cast<unsigned long long>(tally.blocks));
+        if (tally.scales) atomicAdd(A.counters + 1, static_cast<unsigned long long>(tally.scales));
+        if (tally.nibbles) atomicAdd(A.counters + 2, static_cast<unsigned long long>(tally.nibbles));
     }
 }
 
