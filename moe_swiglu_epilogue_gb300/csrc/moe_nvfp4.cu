@@ -951,40 +951,60 @@ swiglu_ex_kernel(const ExArgs X) {
             finish_pass(p0 + lane < n, p0 + lane < n ? cta_begin + q[p0 + lane] : 0);
         __syncwarp();
     };
-    for (;;) {                                              // warp-uniform
+    auto claim = [&]() {                                    // warp-uniform
         int c = 0;
         if (lane == 0) c = atomicAdd(&next_chunk, 1);
         c = __shfl_sync(kFullMask, c, 0);
-        const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
-        if (base >= cta_end) break;
-        uint32_t w[kUnroll][16];
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++) {
-            const int64_t blk = base + 32 * k + lane;
-            if (blk < cta_end) {
-                const uint16_t* p = A.gu + blk * 32;
-                if (kMode == kExCompact) {
-                    // the compact writer (2 output bytes per 4 input bytes)
-                    // streams 8 % faster with plain loads; the quantizing
-                    // modes are faster with the evict-first hint
-                    load_nc_32B(p, w[k]);
-                    load_nc_32B(p + 16, w[k] + 8);
-                } else {
-                    load_stream_32B(p, pol, w[k]);
-                    load_stream_32B(p + 16, pol, w[k] + 8);
-                }
+        return cta_begin + static_cast<int64_t>(c) * kChunk;
+    };
+    auto load_block = [&](int64_t blk, uint32_t* w) {
+        if (blk < cta_end) {
+            const uint16_t* p = A.gu + blk * 32;
+            if (kMode == kExCompact) {
+                // the compact writer (2 output bytes per 4 input bytes)
+                // streams 8 % faster with plain loads; the quantizing
+                // modes are faster with the evict-first hint
+                load_nc_32B(p, w);
+                load_nc_32B(p + 16, w + 8);
             } else {
-#pragma unroll
-                for (int j = 0; j < 16; j++) w[k][j] = 0u;
+                load_stream_32B(p, pol, w);
+                load_stream_32B(p + 16, pol, w + 8);
             }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; j++) w[j] = 0u;
         }
+    };
+    // The compat modes without padded output load one block ahead: the
+    // next chunk's first block is claimed and its loads issued after the
+    // fast passes, so they are in flight while the chunk's blocks are
+    // finished and quantized (the other modes measured slower that way;
+    // with an fp32 clamp the extra registers spill).
+    constexpr bool kPipe = kDefer && kBf16Clamp;
+    static_assert(kUnroll == 2, "two blocks per lane per chunk");
+    uint32_t w0[16], w1[16];
+    int64_t base = 0;
+    if (kPipe) {
+        base = claim();
+        load_block(base + lane, w0);
+    }
+    for (;;) {                                              // warp-uniform
+        if (!kPipe) {
+            base = claim();
+            if (base >= cta_end) break;
+            load_block(base + lane, w0);
+        } else if (base >= cta_end) {
+            break;
+        }
+        load_block(base + 32 + lane, w1);
+        int64_t next = 0;
         if (kMode == kExQuantize) {
 #pragma unroll
             for (int k = 0; k < kUnroll; k++) {
                 const int64_t blk = base + 32 * k + lane;
                 const bool valid = blk < cta_end;
                 float y[16];
-                fast_swiglu16<kBf16Clamp>(A, w[k], y);
+                fast_swiglu16<kBf16Clamp>(A, k ? w1 : w0, y);
                 uint32_t lo, hi, code;
                 scaled_block(X, A.gu + blk * 32, valid, y, lo, hi, code);
                 int64_t oblk;
@@ -1004,10 +1024,14 @@ swiglu_ex_kernel(const ExArgs X) {
 #pragma unroll
             for (int k = 0; k < kUnroll; k++) {
                 float y[16];
-                fast_swiglu16<kBf16Clamp>(A, w[k], y);
-                elems |= bf16_fast_of_block<kTinyTest>(X, base + 32 * k + lane < cta_end, w[k], y,
-                                                                     yb + 8 * k)
+                fast_swiglu16<kBf16Clamp>(A, k ? w1 : w0, y);
+                elems |= bf16_fast_of_block<kTinyTest>(X, base + 32 * k + lane < cta_end, k ? w1 : w0, y,
+                                                       yb + 8 * k)
                          << (16 * k);
+            }
+            if (kPipe) {
+                next = claim();
+                load_block(next + lane, w0);
             }
             if constexpr (!kDefer) {
                 // resolved here: padded output keeps each thread's blocks in
@@ -1039,6 +1063,7 @@ swiglu_ex_kernel(const ExArgs X) {
                 finish_block(blk, blk < cta_end, yb + 8 * k);
             }
         }
+        if (kPipe) base = next;
     }
     if constexpr (kDefer) {
         // the CTA's leftover queues (each under 32 blocks), concatenated in
