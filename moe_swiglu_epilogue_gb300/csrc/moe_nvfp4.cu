@@ -1193,10 +1193,11 @@ nvfp4_quantize_small_kernel(const uint16_t* __restrict__ x, int64_t nblk, float 
 
 enum DequantDivision { kDivNone = 0, kDivMarkstein = 1, kDivIeee = 2 };
 
-// One 16-element block: 8 packed bytes (p), scale value d -> 16 BF16 values.
+// One 16-element block: 8 packed bytes (p), scale value d -> 16 BF16 values,
+// stored with the L2 policy pol.
 template <int kDiv>
 __device__ __forceinline__ void dequantize_block(uint2 p, float d, float gs, float inv_gs,
-                                                 uint16_t* dst16) {
+                                                 uint16_t* dst16, uint64_t pol) {
     uint32_t o[8];
 #pragma unroll
     for (int half = 0; half < 2; half++) {
@@ -1225,13 +1226,13 @@ __device__ __forceinline__ void dequantize_block(uint2 p, float d, float gs, flo
             o[4 * half + k] = bf16x2_rn(v[1], v[0]);
         }
     }
-    store_32B(dst16, o);
+    store_32B_hint(dst16, o, pol);
 }
 
 // Lanes take consecutive pairs of blocks, so every load and store of a warp
 // covers whole 32-byte sectors: 16 packed bytes and 2 scale bytes in, two
-// 32-byte stores out. Two pairs per lane are in flight in each iteration; an
-// odd last block is done at the end.
+// 32-byte stores out. Two pairs per lane per iteration; an odd last block is
+// done at the end.
 template <int kDiv>
 __global__ void __launch_bounds__(kThreads)
 nvfp4_dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ sf,
@@ -1243,10 +1244,13 @@ nvfp4_dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __res
     const int64_t npair = nblk / 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    // The output (4 bytes per element against 0.5625 read) is stored
+    // evict-first: it is larger than L2 at the sizes that matter, and
+    // keeping it there measured 3.6 % slower. The next iteration's loads
+    // are issued before this one's conversion.
     constexpr int kPairs = 2;
-    for (int64_t p0 = tid; p0 < npair; p0 += kPairs * stride) {
-        uint32_t w[kPairs][4];
-        uint32_t s2[kPairs];
+    uint32_t w[kPairs][4], s2[kPairs];
+    auto load_pairs = [&](int64_t p0) {
 #pragma unroll
         for (int k = 0; k < kPairs; k++) {
             const int64_t pi = p0 + k * stride;
@@ -1255,21 +1259,32 @@ nvfp4_dequantize_kernel(const uint8_t* __restrict__ packed, const uint8_t* __res
                 s2[k] = __ldg(reinterpret_cast<const uint16_t*>(sf + 2 * pi));
             }
         }
+    };
+    load_pairs(tid);
+    for (int64_t p0 = tid; p0 < npair; p0 += kPairs * stride) {
+        uint32_t cw[kPairs][4], cs[kPairs];
+#pragma unroll
+        for (int k = 0; k < kPairs; k++) {
+            cs[k] = s2[k];
+#pragma unroll
+            for (int t = 0; t < 4; t++) cw[k][t] = w[k][t];
+        }
+        load_pairs(p0 + kPairs * stride);
 #pragma unroll
         for (int k = 0; k < kPairs; k++) {
             const int64_t pi = p0 + k * stride;
             if (pi < npair) {
-                dequantize_block<kDiv>(make_uint2(w[k][0], w[k][1]), e4m3_value(s2[k] & 0xFFu), gs,
-                                       inv_gs, out + pi * 32);
-                dequantize_block<kDiv>(make_uint2(w[k][2], w[k][3]), e4m3_value(s2[k] >> 8), gs,
-                                       inv_gs, out + pi * 32 + 16);
+                dequantize_block<kDiv>(make_uint2(cw[k][0], cw[k][1]), e4m3_value(cs[k] & 0xFFu), gs,
+                                       inv_gs, out + pi * 32, pol);
+                dequantize_block<kDiv>(make_uint2(cw[k][2], cw[k][3]), e4m3_value(cs[k] >> 8), gs,
+                                       inv_gs, out + pi * 32 + 16, pol);
             }
         }
     }
     if ((nblk & 1) && tid == 0) {
         const int64_t blk = nblk - 1;
         dequantize_block<kDiv>(*reinterpret_cast<const uint2*>(packed + blk * 8), e4m3_value(sf[blk]),
-                               gs, inv_gs, out + blk * 16);
+                               gs, inv_gs, out + blk * 16, pol);
     }
 }
 

@@ -59,6 +59,13 @@ __device__ __forceinline__ void store_32B(void* p, const uint32_t* r) {
                     "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
 }
 
+// The same with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void store_32B_hint(void* p, const uint32_t* r, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+                    "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "l"(pol) : "memory");
+}
+
 // Programmatic dependent launch: wait until the preceding grid in the stream
 // has completed and its memory is visible (a no-op without a programmatic
 // dependency), then let the next grid start launching.
