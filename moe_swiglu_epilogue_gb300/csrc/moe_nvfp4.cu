@@ -1136,23 +1136,28 @@ nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t nblk, float gs,
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnrollQuant;
-    for (int64_t base = warp * 32 * kUnrollQuant; base < nblk; base += step) {
-        uint32_t w[kUnrollQuant][8];
+    // kUnrollQuant blocks per lane per pass, each slot reloaded with the
+    // same block of the next pass as soon as its words are unpacked, so a
+    // lane keeps loads in flight while it quantizes
+    uint32_t w[kUnrollQuant][8];
+    int64_t base = warp * 32 * kUnrollQuant;
+#pragma unroll
+    for (int k = 0; k < kUnrollQuant; k++) {
+        const int64_t blk = base + 32 * k + lane;
+        if (blk < nblk) load_stream_32B(x + blk * 16, pol, w[k]);
+    }
+    for (; base < nblk; base += step) {
 #pragma unroll
         for (int k = 0; k < kUnrollQuant; k++) {
             const int64_t blk = base + 32 * k + lane;
-            if (blk < nblk) load_stream_32B(x + blk * 16, pol, w[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < kUnrollQuant; k++) {
-            const int64_t blk = base + 32 * k + lane;
-            if (blk >= nblk) continue;
             float v[16];
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 v[i] = (i & 1) ? bf16_hi(w[k][i >> 1]) : bf16_lo(w[k][i >> 1]);
                 if (kScaled) v[i] = __fmul_rn(v[i], gs);          // two-level: v = fl(x * gs)
             }
+            if (blk + step < nblk) load_stream_32B(x + (blk + step) * 16, pol, w[k]);
+            if (blk >= nblk) continue;
             uint32_t lo, hi;
             // packed quotient steps (the register budget of 3 CTAs per SM
             // holds them and the 4 blocks in flight without spilling)
