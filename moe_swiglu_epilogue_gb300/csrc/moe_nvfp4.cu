@@ -1324,7 +1324,7 @@ __device__ __forceinline__ void floor_load(const uint32_t* in, int64_t blk, uint
 
 // The fused step's traffic (64 input bytes per block) in its persistent
 // shape: CTA ranges, 64-block chunks claimed from a shared counter, two
-// blocks in flight per lane.
+// blocks per lane, loaded one block ahead as the step does.
 __global__ void __launch_bounds__(kThreads, kMinBlocksFused)
 fused_traffic_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8_t* sf) {
     wait_for_preceding_grid();
@@ -1339,24 +1339,29 @@ fused_traffic_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8_t*
     __shared__ int next_chunk;
     if (threadIdx.x == 0) next_chunk = 0;
     __syncthreads();
-    for (;;) {
+    auto claim = [&]() {                                    // warp-uniform
         int c = 0;
         if (lane == 0) c = atomicAdd(&next_chunk, 1);
         c = __shfl_sync(kFullMask, c, 0);
-        const int64_t base = cta_begin + static_cast<int64_t>(c) * kChunk;
-        if (base >= cta_end) break;
-        uint32_t w[kUnroll][16];
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++)
-            if (base + 32 * k + lane < cta_end) floor_load<16>(in, base + 32 * k + lane, pol, w[k]);
-#pragma unroll
-        for (int k = 0; k < kUnroll; k++)
-            if (base + 32 * k + lane < cta_end) floor_store<16>(w[k], base + 32 * k + lane, packed, sf);
+        return cta_begin + static_cast<int64_t>(c) * kChunk;
+    };
+    static_assert(kUnroll == 2, "two blocks per lane per chunk");
+    uint32_t w0[16], w1[16];
+    int64_t base = claim();
+    if (base + lane < cta_end) floor_load<16>(in, base + lane, pol, w0);
+    while (base < cta_end) {                                // warp-uniform
+        if (base + 32 + lane < cta_end) floor_load<16>(in, base + 32 + lane, pol, w1);
+        if (base + lane < cta_end) floor_store<16>(w0, base + lane, packed, sf);
+        const int64_t next = claim();
+        if (next + lane < cta_end) floor_load<16>(in, next + lane, pol, w0);
+        if (base + 32 + lane < cta_end) floor_store<16>(w1, base + 32 + lane, packed, sf);
+        base = next;
     }
 }
 
 // The quantize-only step's traffic (32 input bytes per block) in its
-// persistent shape: grid-stride, four blocks in flight per lane.
+// persistent shape: grid-stride, four block slots per lane, each reloaded
+// for the next pass as soon as it is read, as the step does.
 __global__ void __launch_bounds__(kThreads, kMinBlocksQuant)
 quantize_traffic_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8_t* sf) {
     wait_for_preceding_grid();
@@ -1365,14 +1370,19 @@ quantize_traffic_kernel(const uint32_t* in, int64_t nblk, uint8_t* packed, uint8
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t step = (static_cast<int64_t>(gridDim.x) * kThreads >> 5) * 32 * kUnrollQuant;
-    for (int64_t base = warp * 32 * kUnrollQuant; base < nblk; base += step) {
-        uint32_t w[kUnrollQuant][8];
+    uint32_t w[kUnrollQuant][8];
+    int64_t base = warp * 32 * kUnrollQuant;
 #pragma unroll
-        for (int k = 0; k < kUnrollQuant; k++)
-            if (base + 32 * k + lane < nblk) floor_load<8>(in, base + 32 * k + lane, pol, w[k]);
+    for (int k = 0; k < kUnrollQuant; k++)
+        if (base + 32 * k + lane < nblk) floor_load<8>(in, base + 32 * k + lane, pol, w[k]);
+    for (; base < nblk; base += step) {
 #pragma unroll
-        for (int k = 0; k < kUnrollQuant; k++)
-            if (base + 32 * k + lane < nblk) floor_store<8>(w[k], base + 32 * k + lane, packed, sf);
+        for (int k = 0; k < kUnrollQuant; k++) {
+            const int64_t blk = base + 32 * k + lane;
+            const uint32_t fold[2] = {xor_fold<4>(w[k]), xor_fold<4>(w[k] + 4)};
+            if (blk + step < nblk) floor_load<8>(in, blk + step, pol, w[k]);
+            if (blk < nblk) floor_store<2>(fold, blk, packed, sf);
+        }
     }
 }
 
