@@ -816,6 +816,72 @@ struct alignas(32) PadSegment {
     int64_t end_blk, lo_blk, hi_blk, shift_blk;
 };
 
+// The two-level step's fast path for one block of each lane of a warp (as
+// fused_block, on v = RN(y gs) with the window widened by the product's
+// roundings): lo / hi / code get the fast nibbles and scale (the scale
+// decided by the definition where the window leaves it open); the elements
+// within the window of a nibble-changing boundary are returned for
+// resolve_chunk_scaled. Every lane calls this together.
+template <bool kBf16Clamp>
+__device__ __forceinline__ uint32_t scaled_fast_block(const ExArgs& X, int64_t blk, bool valid, const uint32_t* w,
+                                                      uint32_t& lo, uint32_t& hi, uint32_t& code_out) {
+    const FusedArgs& A = X.f;
+    const float gs = X.gs;
+    float y[16];
+    fast_swiglu16<kBf16Clamp>(A, w, y);
+    float v[16];
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const float2 vv = __fmul2_rn(make_float2(y[2 * p], y[2 * p + 1]), make_float2(gs, gs));
+        v[2 * p] = vv.x;
+        v[2 * p + 1] = vv.y;
+    }
+    const float amax = abs_max16(v);
+    const float q = amax * kInv6;
+    const uint32_t ends = e4m3x2_rn_sat(q * A.Wp1, q * A.Wm1);
+    uint32_t code = ends & 0xFFu;
+    if (valid && (ends >> 8) != code) {
+        const float lim = amax * (1.0f - 2.0f * A.W);
+        float am = 0.0f;
+        for (int i = 0; i < 16; i++) {
+            if (fabsf(v[i]) >= lim) {
+                float g, u;
+                gate_up_at(A.gu + blk * 32, i, g, u);
+                am = fmaxf(am, fabsf(__fmul_rn(swiglu_precise(g, u, A.L), gs)));
+            }
+        }
+        code = e4m3x2_rn_sat(0.0f, __fdiv_rn(am, 6.0f)) & 0xFFu;
+    }
+    const float d = e4m3_value(code);
+    const float inv = (code == 0u) ? 0.0f : rcp_approx(d);
+    float hs[16];
+    const float closeness = half_steps16(v, inv, hs);
+    lo = e2m1x8(hs);
+    hi = e2m1x8(hs + 8);
+    const bool near = valid && closeness > A.near_fast;
+    uint32_t todo = 0u;
+    if (__any_sync(kFullMask, near) && near) todo = near_boundary_elements(A, v, inv);
+    code_out = code;
+    return todo;
+}
+
+// resolve_nibbles_warp for the two-level step's chunk of a warp (block k of
+// lane l at base + 32 k + l, stored at output block oblk0 / oblk1 for k = 0
+// / 1): each element by RN(definition * gs) under its block's scale. Out of
+// line, as resolve_chunk.
+__device__ __noinline__ void resolve_chunk_scaled(const uint16_t* gu, uint8_t* packed, float L, float gs,
+                                                  int64_t base, int lane, uint32_t mask, uint32_t codes,
+                                                  int64_t oblk0, int64_t oblk1) {
+    resolve_nibbles_warp(
+        lane, mask, codes,
+        [&](int owner, int k, int i, uint32_t code) {
+            float g, u;
+            gate_up_at(gu + (base + 32 * k + owner) * 32, i, g, u);
+            return nibble_by_definition(__fmul_rn(swiglu_precise(g, u, L), gs), e4m3_value(code), code);
+        },
+        [&](int, int, int i, uint32_t nib, int64_t oblk) { patch_nibble(packed + oblk * 8, i, nib); }, oblk0, oblk1);
+}
+
 template <int kMode, bool kBf16Clamp, bool kPadded>
 __global__ void __launch_bounds__(kThreads, kMinBlocksFused)
 swiglu_ex_kernel(const ExArgs X) {
@@ -975,12 +1041,13 @@ swiglu_ex_kernel(const ExArgs X) {
             for (int j = 0; j < 16; j++) w[j] = 0u;
         }
     };
-    // The compat modes without padded output load one block ahead: the
-    // next chunk's first block is claimed and its loads issued after the
-    // fast passes, so they are in flight while the chunk's blocks are
-    // finished and quantized (the other modes measured slower that way;
-    // with an fp32 clamp the extra registers spill).
-    constexpr bool kPipe = kDefer && kBf16Clamp;
+    // Without padded output, the two-level and compat modes load one block
+    // ahead: the next chunk's first block is claimed and its loads issued
+    // after the first block's fast path (two-level) or after the fast passes
+    // (compat), so they are in flight while the chunk is finished (the
+    // padded and compact-writer modes measured slower that way; with an
+    // fp32 clamp the extra registers spill).
+    constexpr bool kPipe = (kDefer || (kMode == kExQuantize && !kPadded)) && kBf16Clamp;
     static_assert(kUnroll == 2, "two blocks per lane per chunk");
     uint32_t w0[16], w1[16];
     int64_t base = 0;
@@ -998,7 +1065,9 @@ swiglu_ex_kernel(const ExArgs X) {
         }
         load_block(base + 32 + lane, w1);
         int64_t next = 0;
-        if (kMode == kExQuantize) {
+        if (kMode == kExQuantize && kPadded) {
+            // padded output: each block decided on its own (the warp-wide
+            // re-decision below measured slower with the segment lookups)
 #pragma unroll
             for (int k = 0; k < kUnroll; k++) {
                 const int64_t blk = base + 32 * k + lane;
@@ -1015,6 +1084,34 @@ swiglu_ex_kernel(const ExArgs X) {
                     A.sf[oblk] = static_cast<uint8_t>(code);
                 }
             }
+        } else if (kMode == kExQuantize) {
+            // fast nibbles stored, then one warp-wide re-decision of the
+            // chunk's elements left to the definition
+            auto two_level_block = [&](int64_t blk, const uint32_t* w, uint32_t& todo, uint32_t& code,
+                                       int64_t& oblk) {
+                const bool valid = blk < cta_end;
+                uint32_t lo, hi;
+                todo = scaled_fast_block<kBf16Clamp>(X, blk, valid, w, lo, hi, code);
+                bool store;
+                out_block(blk, valid, oblk, store);
+                if (store) {
+                    *reinterpret_cast<uint2*>(A.packed + oblk * 8) = make_uint2(lo, hi);
+                    A.sf[oblk] = static_cast<uint8_t>(code);
+                } else {
+                    todo = 0u;
+                }
+            };
+            uint32_t t0, t1, c0, c1;
+            int64_t o0, o1;
+            two_level_block(base + lane, w0, t0, c0, o0);
+            if (kPipe) {
+                next = claim();
+                load_block(next + lane, w0);
+            }
+            two_level_block(base + 32 + lane, w1, t1, c1, o1);
+            const uint32_t mask = t0 | (t1 << 16);
+            if (__any_sync(kFullMask, mask != 0u))
+                resolve_chunk_scaled(A.gu, A.packed, A.L, X.gs, base, lane, mask, c0 | (c1 << 8), o0, o1);
         } else {
             // BF16 values: fast pass over all blocks; blocks with an element
             // whose BF16 rounding the fast value cannot decide are finished
