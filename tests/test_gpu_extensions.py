@@ -369,6 +369,19 @@ def test_full_size_extensions_sampled(name):
     assert np.array_equal(bits(out)[rows], oracle.swiglu_bf16(sub, w.clamp_L))
 
 
+def test_edge_workload_extensions_every_block():
+    """Two-level and BF16 compat on the whole edge workload (16384 rows x
+    I = 4096, 10 % adversarial blocks on and next to rounding ties), every
+    block against the oracle: the warp-wide re-decisions of the two-level
+    step and the queued blocks of compat at their highest rates."""
+    w = W.make("edge")
+    g = dev(w.data)
+    for gs, compat in ((1.25, False), (1.0, True), (1.25, True)):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(g, w.clamp_L, None, gs, compat)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(w.data, w.clamp_L, global_scale=gs, round_bf16=compat)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), (gs, compat)
+
+
 def test_full_size_padded_sampled():
     """Padded output on the full ragged workload, as the benchmark times it
     (256 expert segments, each padded to 128 output rows): sampled input rows
