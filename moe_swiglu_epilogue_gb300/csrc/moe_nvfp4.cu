@@ -607,7 +607,6 @@ struct ExArgs {
     float gate_floor;               // most negative gate the window's bound covers
     uint32_t mid_tol;               // fp32 ulps a BF16 rounding midpoint must be away
     int mid_tol_per_block;          // 1: derive it per block from the most negative gate
-    int tiny_test;                  // 1: the compat modes re-decide results near underflow
 };
 
 // BF16 values of the 16 outputs by the definition (RN_bf16 of the fp32
@@ -630,19 +629,14 @@ __device__ __forceinline__ uint32_t near_bf16_midpoint(float y, uint32_t c16, ui
     return (__float_as_uint(y) * 0x10000u + c16 <= t16) ? 1u : 0u;
 }
 
-// Results near underflow (fast value below 2^-100) are re-decided for
-// kTiny = 2 (the compact writer, whose BF16 values are the output), and for
-// kTiny = 1 when X.tiny_test (the compat modes with a global scale above
-// 2^86; kTiny = 0: the compat mode with global scale 1).
-// There a result whose fast value is below 2^-100 has a definition value
-// of at most 2^-99 with the same sign (the fast path's error there is the
-// window's relative error plus the 2^-150 of an underflowing product), so
-// its v = RN(bf16 * gs) satisfies |v| <= 2^-99 gs <= 2^-13: under a nonzero
-// scale code (d >= 2^-9) it quantizes to a signed zero, it is the block's
-// largest only if every value of the block is, and then the scale code is 0
-// (amax / 6 < 2^-10) and every value quantizes to a signed zero. Its BF16
-// rounding cannot change a byte.
-template <int kTiny>
+// Results near and inside the fp32 subnormal range need no test of their
+// own: for gates at or above the window's floor the fast value's error is
+// the silu's relative error (measured over every BF16 gate, subnormal gates
+// included) plus half an ulp for the product, which rounds as IEEE does
+// when it underflows; below 2^-126 that is at most (k + 1) / 2 + 1 ulps of
+// 2^-149 for a relative bound of k units of 2^-24, inside the tolerance.
+// A BF16 rounding midpoint is still the fp32 value whose low half is
+// 0x8000, so the midpoint test decides them as it decides normal values.
 __device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool valid, const uint32_t* w,
                                                        const float* y, uint32_t* yb) {
     const uint32_t gmin2 = bf16x2_min(bf16x2_min(bf16x2_min(w[0], w[1]), bf16x2_min(w[2], w[3])),
@@ -680,16 +674,9 @@ __device__ __forceinline__ uint32_t bf16_fast_of_block(const ExArgs& X, bool val
             amb |= (near_bf16_midpoint(y[2 * q], c16, t16) << (2 * q)) |
                    (near_bf16_midpoint(y[2 * q + 1], c16, t16) << (2 * q + 1));
     }
-    // block pre-test for the window's range (gates below the floor, results
-    // near underflow); element by element only when it fires
-    bool tiny = false;
-    if (kTiny == 2 || (kTiny == 1 && X.tiny_test)) {
-        float ymin = fabsf(y[0]);
-#pragma unroll
-        for (int i = 1; i < 15; i += 2) ymin = min3(ymin, fabsf(y[i]), fabsf(y[i + 1]));
-        tiny = fminf(ymin, fabsf(y[15])) < 0x1p-100f;
-    }
-    if (gmin < X.gate_floor || tiny) {
+    // block pre-test for the window's range (gates below the floor);
+    // element by element only when it fires
+    if (gmin < X.gate_floor) {
 #pragma unroll
         for (int i = 0; i < 16; i++) {
             const int grp = i >> 3, pw = (i & 7) >> 1;
@@ -919,7 +906,6 @@ swiglu_ex_kernel(const ExArgs X) {
     // each warp's last pass over its queue lengthens the launch more than
     // the queue saves on data with few undecided elements.
     constexpr bool kDefer = (kMode == kExCompat || kMode == kExCompatUnit) && !kPadded;
-    constexpr int kTinyTest = kMode == kExCompact ? 2 : (kMode == kExCompatUnit ? 0 : 1);
     constexpr int kQueue = 31 + 32 * kUnroll;
     __shared__ uint32_t defer_q[kDefer ? kThreads / 32 : 1][kDefer ? kQueue : 1];
     int deferred = 0;                                        // warp-uniform
@@ -1005,7 +991,7 @@ swiglu_ex_kernel(const ExArgs X) {
         float y[16];
         fast_swiglu16<kBf16Clamp>(A, w1, y);
         uint32_t b[8];
-        const uint32_t m = bf16_fast_of_block<kTinyTest>(X, have, w1, y, b);
+        const uint32_t m = bf16_fast_of_block(X, have, w1, y, b);
         resolve_bf16_elements<16>(A, blk, m, b);
         if (have) finish_block(blk, true, b);
     };
@@ -1122,7 +1108,7 @@ swiglu_ex_kernel(const ExArgs X) {
             for (int k = 0; k < kUnroll; k++) {
                 float y[16];
                 fast_swiglu16<kBf16Clamp>(A, k ? w1 : w0, y);
-                elems |= bf16_fast_of_block<kTinyTest>(X, base + 32 * k + lane < cta_end, k ? w1 : w0, y,
+                elems |= bf16_fast_of_block(X, base + 32 * k + lane < cta_end, k ? w1 : w0, y,
                                                        yb + 8 * k)
                          << (16 * k);
             }
@@ -1874,7 +1860,6 @@ int launch_ex(const uint16_t* gu, int64_t rows, int64_t I, float L, const int32_
     X.mid_tol = mid_tol > 32767.0 ? 32767u : static_cast<uint32_t>(mid_tol);
     // the per-gate silu bound was measured with gates clamped at 100
     X.mid_tol_per_block = L <= 100.0f ? 1 : 0;
-    X.tiny_test = gs > 0x1p86f ? 1 : 0;
     const int64_t nblk = rows * (I / 16);
     return launch_status(bf16_bits_of(L) >= 0 ? launch_ex_kernel<true>(X, mode, nblk, di, stream)
                                               : launch_ex_kernel<false>(X, mode, nblk, di, stream));

@@ -224,11 +224,10 @@ def test_compact_writer_and_compat_near_bf16_midpoints():
 
 def test_compact_writer_and_compat_results_near_underflow():
     """Results below 2^-100 (tiny and subnormal BF16 ups or gates): whole
-    blocks of them, and a few of them beside normal results. The compat
-    modes do not re-decide them up to a global scale of 2^86 (they cannot
-    change a byte there); the compact writer does, and so does compat above
-    2^86, where a global scale of 2^110 brings them up to values that
-    matter."""
+    blocks of them, and a few of them beside normal results, through the
+    compact writer and compat at global scales 1, 1.7, 2^86 and 2^110 (where
+    they reach values that matter). No mode re-decides them separately: the
+    BF16 midpoint test decides them as it decides normal values."""
     rng = np.random.default_rng(93)
     nblk = 512
     g = rng.normal(0.0, 2.0, (nblk, 16)).astype(np.float32)
@@ -246,6 +245,37 @@ def test_compact_writer_and_compat_results_near_underflow():
     out = M.moe_swiglu_bf16(dev(gu), 7.0)
     assert np.array_equal(bits(out), oracle.swiglu_bf16(gu, 7.0))
     for gs in (1.0, 1.7, 2.0 ** 86, 2.0 ** 110):
+        p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(gu), 7.0, global_scale=gs, round_to_bf16=True)
+        rp, rs = oracle.swiglu_quantize_nvfp4_ex(gu, 7.0, global_scale=gs, round_bf16=True)
+        assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), gs
+
+
+def test_compact_writer_and_compat_subnormal_results_near_bf16_midpoints():
+    """Results in the fp32 subnormal range and just above it (ups with
+    exponent field 0..3, every BF16 gate with 1/8 <= |g| <= 16) whose fp32
+    value lies within 48 ulps of a BF16 rounding midpoint, found with the
+    oracle: the fast value's error there is the window's relative error plus
+    half an ulp for the underflowing product, and the midpoint test alone
+    must decide them (no separate re-decision of results near underflow)."""
+    allg = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    gv = W.bf16_to_f32(allg)
+    gates = allg[np.isfinite(gv) & (np.abs(gv) <= 16.0) & (np.abs(gv) >= 0.125)]
+    ups = np.array([sg | (e << 7) | m for sg in (0, 0x8000) for e in range(4) for m in range(128)], np.uint16)
+    ups = ups[(ups & 0x7FFF) != 0]
+    g_all = np.repeat(gates, ups.size)
+    u_all = np.tile(ups, gates.size)
+    n = g_all.size - g_all.size % 16
+    y = oracle.swiglu_values(W.interleave_gate_up(g_all[:n].reshape(-1, 16), u_all[:n].reshape(-1, 16)),
+                             7.0).ravel()
+    low = (y.astype(np.float32).view(np.uint32) & 0xFFFF).astype(np.int64)
+    pick = np.flatnonzero((np.abs(low - 0x8000) <= 48) & (y != 0))
+    assert pick.size > 1000 and np.count_nonzero(np.abs(y[pick]) < 2.0 ** -126) > 500
+    pick = pick[:pick.size - pick.size % 16]
+    gu = W.interleave_gate_up(g_all[pick].reshape(-1, 16), u_all[pick].reshape(-1, 16))
+    gu = gu[:gu.shape[0] - gu.shape[0] % 8].reshape(-1, 8 * 32)                # I = 128
+    out = M.moe_swiglu_bf16(dev(gu), 7.0)
+    assert np.array_equal(bits(out), oracle.swiglu_bf16(gu, 7.0))
+    for gs in (1.0, 2.0 ** 110):
         p, s = M.moe_swiglu_nvfp4_quantize_ex(dev(gu), 7.0, global_scale=gs, round_to_bf16=True)
         rp, rs = oracle.swiglu_quantize_nvfp4_ex(gu, 7.0, global_scale=gs, round_bf16=True)
         assert np.array_equal(host(s), rs) and np.array_equal(host(p), rp), gs
