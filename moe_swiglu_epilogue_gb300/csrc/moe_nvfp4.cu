@@ -901,10 +901,9 @@ swiglu_ex_kernel(const ExArgs X) {
     // the compat modes without padded output: each warp's queue of blocks
     // with an element to re-evaluate (at most 31 left plus 32 kUnroll from
     // one chunk), as offsets from cta_begin (the launcher admits fewer than
-    // 2^32 blocks in all). The
-    // compact writer resolves in place: it streams near the copy floor, where
-    // each warp's last pass over its queue lengthens the launch more than
-    // the queue saves on data with few undecided elements.
+    // 2^32 blocks in all). The compact writer resolves in place: it streams
+    // near the copy floor, where the passes over a queue lengthen the launch
+    // more than the queue saves on data with few undecided elements.
     constexpr bool kDefer = (kMode == kExCompat || kMode == kExCompatUnit) && !kPadded;
     constexpr int kQueue = 31 + 32 * kUnroll;
     __shared__ uint32_t defer_q[kDefer ? kThreads / 32 : 1][kDefer ? kQueue : 1];
